@@ -1,0 +1,35 @@
+"""Oracle for prefix-tree ("tree training") attention — TEST INFRASTRUCTURE ONLY.
+
+This package is a plain, slow, obviously-correct CPU restatement of what the
+packed-trie attention path computes.  It exists to check the CUDA library and
+nothing else: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import it.
+The product package never imports it, and it imports nothing from the product
+package (they share only the seeded input generators in ``workloads/``).
+
+Sources (web pages; cited by title and section):
+
+* "AReaL Tree Training 完全指南" (AReaL Tree Training guide), sections
+  "树构建流程" (tree construction: FFD greedy packing, trie compression),
+  "核心数据结构：TrieNode" (node spans, preorder ``nodes`` list, virtual root),
+  "打包数据的生成" (position ids from the dense mask), the packing figure
+  (ancestor mask, worked example [A,B,C,D]/[A,B,E,F]/[A,G,H]),
+  "FlexAttention + BlockMask" (128-token blocks) and
+  "参数背后的源码校验逻辑" (packing validation).
+* "AREAL-DTA: Dynamic Tree Attention for Efficient Reinforcement Learning of
+  Large Language Models", section 3 "Problem formalisation" (total loss is the
+  sum of per-sequence losses; a shared prefix is computed once and its
+  gradient sums the contributions of every descendant sequence).
+
+Modules:
+
+* ``oracle.trie``      — trie insertion, first-fit-decreasing packing,
+                         compression, preorder layout, 128-padding.
+* ``oracle.mask``      — dense ancestor mask by parent-pointer walks,
+                         position ids, 128x128 tile classes.
+* ``oracle.attention`` — masked softmax attention forward/backward in fp64.
+
+Every floating-point routine accumulates in float64 on inputs that were
+already rounded to bf16 by the caller.  Parity status of each function is
+stated in its module header.
+"""

@@ -1,0 +1,272 @@
+/*
+ * tree_attn.h — C ABI of the packed prefix-trie ("tree training") attention
+ * library for NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes.  Sequences that share prefixes (n_samples
+ * responses to one prompt, a shared system prompt, a shared multi-turn
+ * history) are packed once into a compressed trie laid out in preorder, so
+ * every shared token is stored and computed once (AReaL Tree Training guide,
+ * sections "什么是 Tree Training" and "树构建流程").  Token i attends to
+ * token j iff j <= i and j's node is i's node or one of its ancestors (the
+ * guide's packing figure), and the position id of a token is the number of
+ * tokens it may attend to minus one (section "打包数据的生成").  Attention is
+ * ordinary softmax attention under that mask; its backward pass sums the
+ * gradient of a shared-prefix token over every continuation (AREAL-DTA,
+ * section 3 "Problem formalisation").
+ *
+ * Data model at this boundary.
+ *   token_node[T_pad]   node of each packed token, -1 for a pad token.
+ *   node_entry[N]       preorder rank of each node (a permutation of 0..N-1).
+ *   node_exit[N]        largest preorder rank inside the node's subtree.
+ *   Node a is an ancestor-or-self of node b iff
+ *       node_entry[a] <= node_entry[b] <= node_exit[a].
+ *   Tokens are laid out in preorder: each node's tokens are contiguous and
+ *   nodes appear in increasing rank (the guide's TrieNode start_idx/end_idx
+ *   spans and root-level preorder `nodes` list).  Several tries may share one
+ *   buffer (a forest under a virtual root).  Pad tokens may sit only outside
+ *   every subtree's token span (between top-level subtrees or at the end).
+ *   T_pad is a multiple of the 128-token block (section "FlexAttention +
+ *   BlockMask"; block-alignment check of "参数背后的源码校验逻辑").
+ *
+ *   Q, O, dO, dQ  bf16 [T_pad, Hq, d]   (token-major, d innermost, batch 1)
+ *   K, V, dK, dV  bf16 [T_pad, Hkv, d]
+ *   LSE           fp32 [Hq, T_pad]      natural-log logsumexp per row
+ *   Query head h reads key/value head h / (Hq / Hkv).
+ *
+ * Pad semantics: a pad token attends to nothing and is attended by nothing;
+ * its O and LSE are 0 and -inf, its gradients 0, its position id 0.
+ *
+ * Conventions for every call.
+ *  * Ownership: the caller owns every buffer.  The library never allocates,
+ *    frees or synchronises; work is queued on `stream` and runs in stream
+ *    order.  Device pointers must be 16-byte aligned.
+ *  * Errors detectable from the arguments (null pointer, sizes, alignment,
+ *    unsupported shapes, short workspace) are returned synchronously and
+ *    nothing is launched.  A launch failure returns TREE_ERR_CUDA.
+ *  * Errors that depend on device data (a malformed tree; a device-side wait
+ *    that ran out of time) are written to `*dev_status` (device int32).  The
+ *    caller zeroes it once; the first error sticks, and later kernels that
+ *    find it non-zero skip their work.  Read it after synchronising.
+ */
+#ifndef TREE_ATTN_H_
+#define TREE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TREE_API __attribute__((visibility("default")))
+#else
+#define TREE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tree_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  TREE_OK = 0,
+  TREE_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad head split */
+  TREE_ERR_ALIGNMENT = 2,      /* T_pad or a capacity not a multiple of 128; unaligned pointer */
+  TREE_ERR_CAPACITY = 3,       /* a sequence longer than max_tokens_per_mb */
+  TREE_ERR_MALFORMED_TREE = 4, /* token_node/node_entry/node_exit inconsistent (device-detected) */
+  TREE_ERR_UNSUPPORTED = 5,    /* block != 128, head_dim not in {64,128} */
+  TREE_ERR_CUDA = 6,           /* a CUDA call or launch failed */
+  TREE_ERR_TIMEOUT = 7,        /* a device-side wait exceeded its limit (device-detected) */
+  TREE_ERR_WORKSPACE = 8       /* workspace or blockmap buffer too small */
+} tree_status_t;
+
+/* Human-readable name of a status code (static string). */
+TREE_API const char* tree_status_string(int status);
+
+/* Library version as "major.minor.patch". */
+TREE_API const char* tree_version(void);
+
+/* ------------------------------------------------------------------------
+ * tree_pack_positions — per-key reach and position ids.
+ *
+ * Source: the guide's section "打包数据的生成" (position id = attendable
+ * count - 1) and its packing figure (ancestor mask).  For a preorder layout
+ * the mask has the interval form  M(i,j) = (j <= i <= key_reach[j]),  where
+ * key_reach[j] is the last token of the subtree of node(j); hence
+ * position_ids is an inclusive scan of +1 at j and -1 after key_reach[j].
+ *
+ *   token_node   [in]  device int32[T_pad]
+ *   node_entry   [in]  device int32[n_nodes]   (may be NULL if n_nodes == 0)
+ *   node_exit    [in]  device int32[n_nodes]
+ *   position_ids [out] device int32[T_pad]; pads get 0
+ *   key_reach    [out] device int32[T_pad]; pads get j - 1 (empty interval)
+ *   workspace    [tmp] device, >= tree_pack_positions_workspace_bytes()
+ *   dev_status   [out] device int32; TREE_ERR_MALFORMED_TREE when a node
+ *                      id is out of range, ranks are not a permutation,
+ *                      exit < entry, a node is empty or split, nodes are not
+ *                      in rank order, subtree intervals cross, or a pad sits
+ *                      inside a subtree's span.
+ * Returns TREE_ERR_ALIGNMENT if T_pad % 128 != 0.  T_pad == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+TREE_API size_t tree_pack_positions_workspace_bytes(int32_t T_pad, int32_t n_nodes);
+TREE_API tree_status_t tree_pack_positions(const int32_t* token_node, int32_t T_pad,
+                                  const int32_t* node_entry, const int32_t* node_exit,
+                                  int32_t n_nodes, int32_t* position_ids, int32_t* key_reach,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                  tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * tree_blockmap_build — classify every 128x128 (query block, key block)
+ * tile as EMPTY, FULL or PARTIAL and list the non-empty tiles.
+ *
+ * Source: the guide's sections "树构建流程" step 4 and "FlexAttention +
+ * BlockMask" (a block mask over 128-token blocks built from the trie).  From
+ * the interval form of the mask, for key block kb with per-block
+ * mn = min key_reach, mx = max key_reach (pads included):
+ *   tile (qa, kb), kb > qa : EMPTY
+ *   tile (kb, kb)          : PARTIAL if the block holds a real key, else EMPTY
+ *   tile (qa, kb), kb < qa : EMPTY if mx < 128*qa, FULL if mn >= 128*qa+127,
+ *                            else PARTIAL.
+ * So each key block's non-empty tiles form one column run
+ *   qa = kb (PARTIAL), kb < qa <= col_full_hi (FULL), col_full_hi < qa <= col_hi (PARTIAL).
+ *
+ *   key_reach [in]  device int32[T_pad] from tree_pack_positions
+ *   block     [in]  must be 128 (else TREE_ERR_UNSUPPORTED)
+ *   blockmap  [out] device buffer of >= tree_blockmap_bytes(T_pad) bytes,
+ *                   int32 words laid out as (nb = T_pad / 128):
+ *     [0]                   nb
+ *     [1]                   nnz (non-empty tiles)
+ *     [2], [3]              reserved (0)
+ *     col_full_hi[nb]       at 4
+ *     col_hi[nb]            at 4 + nb        (kb - 1 when the column is empty)
+ *     row_cnt[nb]           at 4 + 2nb       non-empty tiles of query block qa
+ *     row_nfull[nb]         at 4 + 3nb       FULL tiles of query block qa
+ *     row_ptr[nb + 1]       at 4 + 4nb       CSR offsets into row_idx
+ *     row_order[nb]         at 5 + 5nb       query blocks by row_cnt descending
+ *                                            (ties: smaller index first)
+ *     col_order[nb]         at 5 + 6nb       key blocks by column length
+ *                                            descending (ties: smaller first)
+ *     row_idx[nnz]          at 5 + 7nb       per query block: its FULL key
+ *                                            blocks ascending, then its
+ *                                            PARTIAL key blocks ascending
+ * ---------------------------------------------------------------------- */
+TREE_API size_t tree_blockmap_bytes(int32_t T_pad);
+TREE_API tree_status_t tree_blockmap_build(const int32_t* key_reach, int32_t T_pad, int32_t block,
+                                  void* blockmap, size_t blockmap_bytes, int32_t* dev_status,
+                                  tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * tree_attn_fwd — tree-masked softmax attention forward.
+ *
+ * Source: the guide's packing figure and section "两种注意力实现"
+ * (attention under the tree mask in 128-token blocks, batch 1).  For each
+ * query head h and query row i:
+ *   O[i,h] = sum_j P_ij V[j, h/g],  P = softmax_j(scale * Q[i,h].K[j,h/g])
+ * over the j with M(i,j); LSE[h,i] = log sum_j exp(scale * Q[i,h].K[j,h/g]).
+ * EMPTY tiles are skipped; the mask is evaluated only on PARTIAL tiles.
+ * bf16 inputs, fp32 accumulation, P rounded to bf16 before P.V, O rounded
+ * to bf16 (nearest even).
+ *
+ *   q, k, v   [in]  device bf16 (layouts above)
+ *   key_reach [in]  device int32[T_pad]
+ *   blockmap  [in]  from tree_blockmap_build for the same key_reach
+ *   d         [in]  64 or 128; Hq % Hkv == 0
+ *   scale     [in]  softmax scale (1/sqrt(d) is the usual choice)
+ *   o         [out] device bf16 [T_pad, Hq, d]
+ *   lse       [out] device fp32 [Hq, T_pad]
+ *   dev_status[out] TREE_ERR_TIMEOUT if a device wait ran out of time
+ * ---------------------------------------------------------------------- */
+TREE_API tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v,
+                            const int32_t* key_reach, const void* blockmap, int32_t T_pad,
+                            int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o,
+                            float* lse, int32_t* dev_status, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * tree_attn_bwd — backward of tree_attn_fwd.
+ *
+ * Source: AREAL-DTA section 3 "Problem formalisation" (the loss is a sum over
+ * sequences; a shared prefix is processed once and its gradient accumulates
+ * every descendant sequence's contribution).  With P recomputed from LSE:
+ *   D_i  = sum_d dO[i,h,d] O[i,h,d]
+ *   dS   = P * (dO V^T - D)
+ *   dQ   = scale * dS K,   dK = scale * dS^T Q (summed over the g heads of a
+ *   kv head),             dV = P^T dO          (summed likewise).
+ * A shared-prefix key is visible to the queries of every continuation, so
+ * its dK/dV sum over all of them by construction.
+ *
+ *   o, d_o, lse   [in]  forward output, upstream gradient, forward LSE
+ *   dq            [out] device bf16 [T_pad, Hq, d]
+ *   dk, dv        [out] device bf16 [T_pad, Hkv, d]
+ *   workspace     [tmp] >= tree_attn_bwd_workspace_bytes(T_pad, Hq, d):
+ *                       fp32 dQ accumulator + fp32 D rows
+ * ---------------------------------------------------------------------- */
+TREE_API size_t tree_attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d);
+TREE_API tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                            const void* d_o, const float* lse, const int32_t* key_reach,
+                            const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
+                            int32_t d, float scale, void* dq, void* dk, void* dv,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Host packer: sequences -> tries in the layout above.
+ *
+ * Source: the guide's section "树构建流程": first-fit-decreasing greedy
+ * insertion (longest first; a sequence joins the first trie whose occupied
+ * node count plus the nodes it adds stays within max_tokens_per_mb, else
+ * opens a new trie), compression of single-child chains whose passing
+ * sequences are identical, preorder flattening under a virtual root, and
+ * padding to a multiple of `block` (or to max_tokens_per_mb when
+ * pad_to_max != 0).  Validation follows "参数背后的源码校验逻辑":
+ * max_tokens_per_mb must be positive (TREE_ERR_INVALID_ARG) and a multiple
+ * of block (TREE_ERR_ALIGNMENT); a sequence longer than max_tokens_per_mb
+ * is TREE_ERR_CAPACITY; an empty sequence is TREE_ERR_INVALID_ARG.
+ * Children keep first-insertion order; ties in length keep input order.
+ * All pointers are host pointers.  The packing object is owned by the
+ * caller and released with tree_packing_free.
+ * ---------------------------------------------------------------------- */
+typedef struct tree_packing tree_packing_t;
+
+TREE_API tree_status_t tree_packing_build(const int32_t* tokens, const int64_t* seq_offsets,
+                                 int32_t n_seqs, int32_t max_tokens_per_mb, int32_t block,
+                                 int32_t pad_to_max, tree_packing_t** out);
+TREE_API void tree_packing_free(tree_packing_t* packing);
+TREE_API int32_t tree_packing_num_tries(const tree_packing_t* packing);
+
+/* Sizes of trie t: real tokens, padded length, nodes, sequences, and the
+ * number of visible (i, j) pairs = sum over real tokens of (position + 1). */
+TREE_API tree_status_t tree_packing_trie_info(const tree_packing_t* packing, int32_t t,
+                                     int32_t* n_tokens, int32_t* T_pad, int32_t* n_nodes,
+                                     int32_t* n_seqs, int64_t* visible_pairs);
+
+/* Arrays of trie t (host buffers sized from tree_packing_trie_info; any may
+ * be NULL to skip it): token_node[T_pad], token_ids[T_pad] (-1 for pads),
+ * node_entry[n_nodes], node_exit[n_nodes], seq_ids[n_seqs] (input indices in
+ * insertion order). */
+TREE_API tree_status_t tree_packing_trie_arrays(const tree_packing_t* packing, int32_t t,
+                                       int32_t* token_node, int32_t* token_ids,
+                                       int32_t* node_entry, int32_t* node_exit,
+                                       int32_t* seq_ids);
+
+/* Packed token indices of the k-th sequence of trie t, in sequence order
+ * (the spans of the nodes it passes, concatenated); `out` holds the
+ * sequence's length. */
+TREE_API tree_status_t tree_packing_seq_indices(const tree_packing_t* packing, int32_t t, int32_t k,
+                                       int32_t* out, int32_t capacity);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.
+ *
+ * tree_debug_wait_timeout — launch one warp that waits on a shared-memory
+ * barrier nothing ever arrives on, through the same bounded wait that guards
+ * every pipeline wait in tree_attn_fwd/bwd.  After limit_ns (1 ms .. 2 s,
+ * else TREE_ERR_INVALID_ARG) the wait gives up and TREE_ERR_TIMEOUT is
+ * written to *dev_status (unless it already holds an error); the kernel then
+ * returns normally.  This is how the failure-detection path is tested
+ * without faulting or hanging a GPU.  The pages have no counterpart.
+ * ---------------------------------------------------------------------- */
+TREE_API tree_status_t tree_debug_wait_timeout(int32_t* dev_status, int64_t limit_ns,
+                                               tree_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TREE_ATTN_H_ */

@@ -1,0 +1,285 @@
+"""Python binding of ``libtreeattn`` — packed prefix-trie attention for GB300.
+
+Argument marshalling only: every step of the hot path runs in the library's
+sm_103a kernels (``include/tree_attn.h``).  PyTorch provides device memory
+and streams.  There is no fallback: if the compiled library is missing the
+import fails loudly; build it with ``python prefix_tree_attention_gb300/build.py``.
+
+Entry points mirror the C ABI names: ``tree_pack_positions``,
+``tree_blockmap_build``, ``tree_attn_fwd``, ``tree_attn_bwd`` (each takes
+tensors, checks their dtype/shape/device, passes raw pointers and the current
+CUDA stream, and raises ``TreeError`` on a non-OK status), plus the host
+packer ``pack_sequences``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libtreeattn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python prefix_tree_attention_gb300/build.py`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_P, _I32, _I64, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+_sig = {
+    "tree_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "tree_version": (ctypes.c_char_p, []),
+    "tree_pack_positions_workspace_bytes": (_SZ, [_I32, _I32]),
+    "tree_pack_positions": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P, _P]),
+    "tree_blockmap_bytes": (_SZ, [_I32]),
+    "tree_blockmap_build": (ctypes.c_int, [_P, _I32, _I32, _P, _SZ, _P, _P]),
+    "tree_attn_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _P, _P,
+                                     _P, _P]),
+    "tree_attn_bwd_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
+    "tree_attn_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
+                                     _F32, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tree_packing_build": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _P]),
+    "tree_packing_free": (None, [_P]),
+    "tree_packing_num_tries": (_I32, [_P]),
+    "tree_packing_trie_info": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P]),
+    "tree_packing_trie_arrays": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P]),
+    "tree_packing_seq_indices": (ctypes.c_int, [_P, _I32, _I32, _P, _I32]),
+    "tree_debug_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
+}
+for _name, (_res, _args) in _sig.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+EXPORTED_SYMBOLS = tuple(_sig)
+
+TREE_OK = 0
+BLOCK = 128
+
+
+class TreeError(RuntimeError):
+    """A non-OK status returned by the library."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} ({status})")
+
+
+def status_string(status: int) -> str:
+    return _lib.tree_status_string(int(status)).decode()
+
+
+def version() -> str:
+    return _lib.tree_version().decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != TREE_OK:
+        raise TreeError(fn, status)
+
+
+def _stream_ptr(stream=None) -> int:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _need(t, dtype, name):
+    import torch
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    del torch
+
+
+# --------------------------------------------------------------- workspaces
+def pack_positions_workspace_bytes(T_pad: int, n_nodes: int) -> int:
+    return int(_lib.tree_pack_positions_workspace_bytes(T_pad, n_nodes))
+
+
+def blockmap_bytes(T_pad: int) -> int:
+    return int(_lib.tree_blockmap_bytes(T_pad))
+
+
+def attn_bwd_workspace_bytes(T_pad: int, Hq: int, d: int) -> int:
+    return int(_lib.tree_attn_bwd_workspace_bytes(T_pad, Hq, d))
+
+
+# --------------------------------------------------------------- hot path
+def tree_pack_positions(token_node, node_entry, node_exit, position_ids, key_reach, workspace,
+                        dev_status, stream=None):
+    import torch
+    _need(token_node, torch.int32, "token_node")
+    for t, n in ((position_ids, "position_ids"), (key_reach, "key_reach")):
+        _need(t, torch.int32, n)
+    T_pad = token_node.numel()
+    N = node_entry.numel()
+    _check("tree_pack_positions", _lib.tree_pack_positions(
+        _ptr(token_node), T_pad, _ptr(node_entry) if N else 0, _ptr(node_exit) if N else 0, N,
+        _ptr(position_ids), _ptr(key_reach), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream_ptr(stream)))
+
+
+def tree_blockmap_build(key_reach, blockmap, dev_status, stream=None, block: int = BLOCK):
+    import torch
+    _need(key_reach, torch.int32, "key_reach")
+    _check("tree_blockmap_build", _lib.tree_blockmap_build(
+        _ptr(key_reach), key_reach.numel(), block, _ptr(blockmap),
+        blockmap.numel() * blockmap.element_size(), _ptr(dev_status), _stream_ptr(stream)))
+
+
+def tree_attn_fwd(q, k, v, key_reach, blockmap, o, lse, dev_status, scale=None, stream=None):
+    import torch
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    if k.shape != (T, Hkv, d) or v.shape != k.shape or o.shape != q.shape or lse.shape != (Hq, T):
+        raise ValueError("shape mismatch")
+    scale = d ** -0.5 if scale is None else float(scale)
+    _check("tree_attn_fwd", _lib.tree_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(key_reach), _ptr(blockmap), T, Hq, Hkv, d, scale,
+        _ptr(o), _ptr(lse), _ptr(dev_status), _stream_ptr(stream)))
+
+
+def tree_attn_bwd(q, k, v, o, d_o, lse, key_reach, blockmap, dq, dk, dv, workspace, dev_status,
+                  scale=None, stream=None):
+    import torch
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (d_o, "d_o"), (dq, "dq"), (dk, "dk"),
+                 (dv, "dv")):
+        _need(t, torch.bfloat16, n)
+    if dk.shape != k.shape or dv.shape != v.shape or dq.shape != q.shape or d_o.shape != q.shape:
+        raise ValueError("shape mismatch")
+    scale = d ** -0.5 if scale is None else float(scale)
+    _check("tree_attn_bwd", _lib.tree_attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o), _ptr(lse), _ptr(key_reach),
+        _ptr(blockmap), T, Hq, Hkv, d, scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream_ptr(stream)))
+
+
+def tree_debug_wait_timeout(dev_status, limit_ns: int, stream=None):
+    """Run the bounded-wait probe; TREE_ERR_TIMEOUT lands in dev_status."""
+    _check("tree_debug_wait_timeout", _lib.tree_debug_wait_timeout(
+        _ptr(dev_status), int(limit_ns), _stream_ptr(stream)))
+
+
+# --------------------------------------------------------------- host packer
+@dataclass
+class Trie:
+    """One packed trie from the host packer (numpy int32 arrays)."""
+
+    n_tokens: int
+    T_pad: int
+    n_nodes: int
+    visible_pairs: int
+    token_node: np.ndarray
+    token_ids: np.ndarray
+    node_entry: np.ndarray
+    node_exit: np.ndarray
+    seq_ids: list
+    seq_index: dict      # input sequence index -> packed token indices
+
+
+def pack_sequences(seqs, max_tokens_per_mb: int, block: int = BLOCK, pad_to_max: bool = False):
+    """Pack token sequences into tries with the library's host packer."""
+    lens = np.array([len(s) for s in seqs], dtype=np.int64)
+    offs = np.zeros(len(seqs) + 1, dtype=np.int64)
+    np.cumsum(lens, out=offs[1:])
+    flat = np.zeros(max(1, int(offs[-1])), dtype=np.int32)
+    for i, s in enumerate(seqs):
+        flat[offs[i]:offs[i + 1]] = s
+    handle = ctypes.c_void_p()
+    _check("tree_packing_build", _lib.tree_packing_build(
+        flat.ctypes.data, offs.ctypes.data, len(seqs), int(max_tokens_per_mb), int(block),
+        1 if pad_to_max else 0, ctypes.byref(handle)))
+    try:
+        out = []
+        for t in range(_lib.tree_packing_num_tries(handle)):
+            nt, tp, nn, ns = (ctypes.c_int32() for _ in range(4))
+            pairs = ctypes.c_int64()
+            _check("tree_packing_trie_info", _lib.tree_packing_trie_info(
+                handle, t, ctypes.byref(nt), ctypes.byref(tp), ctypes.byref(nn),
+                ctypes.byref(ns), ctypes.byref(pairs)))
+            token_node = np.empty(tp.value, np.int32)
+            token_ids = np.empty(tp.value, np.int32)
+            entry = np.empty(nn.value, np.int32)
+            exit_ = np.empty(nn.value, np.int32)
+            sids = np.empty(ns.value, np.int32)
+            _check("tree_packing_trie_arrays", _lib.tree_packing_trie_arrays(
+                handle, t, token_node.ctypes.data, token_ids.ctypes.data, entry.ctypes.data,
+                exit_.ctypes.data, sids.ctypes.data))
+            seq_index = {}
+            for k_, sid in enumerate(sids.tolist()):
+                idx = np.empty(len(seqs[sid]), np.int32)
+                _check("tree_packing_seq_indices", _lib.tree_packing_seq_indices(
+                    handle, t, k_, idx.ctypes.data, idx.size))
+                seq_index[sid] = idx
+            out.append(Trie(nt.value, tp.value, nn.value, pairs.value, token_node, token_ids,
+                            entry, exit_, sids.tolist(), seq_index))
+        return out
+    finally:
+        _lib.tree_packing_free(handle)
+
+
+# --------------------------------------------------------------- convenience
+class TrieBuffers:
+    """Device buffers for one trie: positions, reach, blockmap, workspaces.
+
+    Allocates with torch once; every call after that only launches kernels.
+    """
+
+    def __init__(self, T_pad: int, n_nodes: int, Hq: int, d: int, device="cuda"):
+        import torch
+        self.T_pad, self.n_nodes, self.Hq, self.d = T_pad, n_nodes, Hq, d
+        i32 = dict(dtype=torch.int32, device=device)
+        self.position_ids = torch.empty(T_pad, **i32)
+        self.key_reach = torch.empty(T_pad, **i32)
+        self.pos_ws = torch.empty((pack_positions_workspace_bytes(T_pad, n_nodes) + 3) // 4, **i32)
+        self.blockmap = torch.empty((blockmap_bytes(T_pad) + 3) // 4, **i32)
+        self.bwd_ws = torch.empty((attn_bwd_workspace_bytes(T_pad, Hq, d) + 3) // 4,
+                                  dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, **i32)
+
+
+def blockmap_view(blockmap_words: np.ndarray) -> dict:
+    """Decode a blockmap buffer (host copy, int32 words) into its fields."""
+    nb = int(blockmap_words[0])
+    w = blockmap_words
+    nnz = int(w[1])
+    col_full_hi = w[4:4 + nb]
+    col_hi = w[4 + nb:4 + 2 * nb]
+    row_cnt = w[4 + 2 * nb:4 + 3 * nb]
+    row_nfull = w[4 + 3 * nb:4 + 4 * nb]
+    row_ptr = w[4 + 4 * nb:5 + 5 * nb]
+    row_order = w[5 + 5 * nb:5 + 6 * nb]
+    col_order = w[5 + 6 * nb:5 + 7 * nb]
+    row_idx = w[5 + 7 * nb:5 + 7 * nb + nnz]
+    return dict(nb=nb, nnz=nnz, col_full_hi=col_full_hi, col_hi=col_hi, row_cnt=row_cnt,
+                row_nfull=row_nfull, row_ptr=row_ptr, row_order=row_order, col_order=col_order,
+                row_idx=row_idx)
+
+
+def tile_classes_from_blockmap(view: dict) -> np.ndarray:
+    """Dense uint8[nb, nb] tile classes (0 EMPTY, 1 FULL, 2 PARTIAL) expanded
+    from the blockmap's per-column runs."""
+    nb = view["nb"]
+    cls = np.zeros((nb, nb), np.uint8)
+    for kb in range(nb):
+        hi, fh = int(view["col_hi"][kb]), int(view["col_full_hi"][kb])
+        for qa in range(kb, hi + 1):
+            cls[qa, kb] = 2 if (qa == kb or qa > fh) else 1
+    return cls

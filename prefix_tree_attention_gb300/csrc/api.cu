@@ -1,0 +1,197 @@
+// C ABI of the library (declared in include/tree_attn.h): argument checks,
+// TMA tensor-map encoding and kernel launches.  No allocation, no
+// synchronisation: every call only queues work on the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace tree {
+cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const int32_t* key_reach, const void* blockmap, int32_t T_pad,
+                            int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o, float* lse,
+                            int32_t* status, cudaStream_t s);
+size_t attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d);
+cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const void* o, const void* d_o,
+                            const float* lse, const int32_t* key_reach, const void* blockmap,
+                            int32_t T_pad, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                            void* dq, void* dk, void* dv, void* workspace, int32_t* status,
+                            cudaStream_t s, int num_sms);
+}  // namespace tree
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The driver's tensor-map encoder, resolved once through the runtime so the
+// library itself does not link libcuda (it loads on machines without a GPU).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Token-major [T, H, d] bf16 tensor viewed as a 3-D TMA map with a
+// 64-element (128-byte) x 1 head x 128-token box, 128-byte swizzle.
+bool encode_map(CUtensorMap* map, const void* base, int32_t T, int32_t H, int32_t d) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(tree::kBlock)};
+  cuuint32_t elem[3] = {1, 1, 1};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                                      const_cast<void*>(base), dims, strides, box, elem,
+                                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms_current() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+tree_status_t check_attn_shape(int32_t T_pad, int32_t Hq, int32_t Hkv, int32_t d) {
+  if (T_pad < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return TREE_ERR_INVALID_ARG;
+  if (T_pad % tree::kBlock) return TREE_ERR_ALIGNMENT;
+  if (d != 64 && d != 128) return TREE_ERR_UNSUPPORTED;
+  return TREE_OK;
+}
+
+tree_status_t cuda_result(cudaError_t e) { return e == cudaSuccess ? TREE_OK : TREE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* tree_status_string(int status) {
+  switch (status) {
+    case TREE_OK: return "TREE_OK";
+    case TREE_ERR_INVALID_ARG: return "TREE_ERR_INVALID_ARG";
+    case TREE_ERR_ALIGNMENT: return "TREE_ERR_ALIGNMENT";
+    case TREE_ERR_CAPACITY: return "TREE_ERR_CAPACITY";
+    case TREE_ERR_MALFORMED_TREE: return "TREE_ERR_MALFORMED_TREE";
+    case TREE_ERR_UNSUPPORTED: return "TREE_ERR_UNSUPPORTED";
+    case TREE_ERR_CUDA: return "TREE_ERR_CUDA";
+    case TREE_ERR_TIMEOUT: return "TREE_ERR_TIMEOUT";
+    case TREE_ERR_WORKSPACE: return "TREE_ERR_WORKSPACE";
+    default: return "TREE_ERR_UNKNOWN";
+  }
+}
+
+const char* tree_version(void) { return "0.1.0"; }
+
+size_t tree_pack_positions_workspace_bytes(int32_t T_pad, int32_t n_nodes) {
+  if (T_pad < 0 || n_nodes < 0) return 0;
+  return tree::pack_positions_workspace_bytes(T_pad, n_nodes);
+}
+
+tree_status_t tree_pack_positions(const int32_t* token_node, int32_t T_pad,
+                                  const int32_t* node_entry, const int32_t* node_exit,
+                                  int32_t n_nodes, int32_t* position_ids, int32_t* key_reach,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                  tree_stream_t stream) {
+  if (T_pad < 0 || n_nodes < 0 || !dev_status) return TREE_ERR_INVALID_ARG;
+  if (T_pad % tree::kBlock) return TREE_ERR_ALIGNMENT;
+  if (T_pad == 0) return TREE_OK;
+  if (!token_node || !position_ids || !key_reach || !workspace ||
+      (n_nodes > 0 && (!node_entry || !node_exit)))
+    return TREE_ERR_INVALID_ARG;
+  if (n_nodes > T_pad) return TREE_ERR_INVALID_ARG;   // every node owns >= 1 token
+  if (!aligned16(workspace)) return TREE_ERR_ALIGNMENT;
+  if (workspace_bytes < tree::pack_positions_workspace_bytes(T_pad, n_nodes))
+    return TREE_ERR_WORKSPACE;
+  return cuda_result(tree::launch_pack_positions(token_node, T_pad, node_entry, node_exit,
+                                                 n_nodes, position_ids, key_reach, workspace,
+                                                 dev_status, stream));
+}
+
+size_t tree_blockmap_bytes(int32_t T_pad) {
+  if (T_pad < 0) return 0;
+  return sizeof(int32_t) * tree::blockmap_words(T_pad / tree::kBlock);
+}
+
+tree_status_t tree_blockmap_build(const int32_t* key_reach, int32_t T_pad, int32_t block,
+                                  void* blockmap, size_t blockmap_bytes, int32_t* dev_status,
+                                  tree_stream_t stream) {
+  if (T_pad < 0 || !dev_status) return TREE_ERR_INVALID_ARG;
+  if (block != tree::kBlock) return TREE_ERR_UNSUPPORTED;
+  if (T_pad % tree::kBlock) return TREE_ERR_ALIGNMENT;
+  if (T_pad == 0) return TREE_OK;
+  if (!key_reach || !blockmap) return TREE_ERR_INVALID_ARG;
+  if (!aligned16(blockmap)) return TREE_ERR_ALIGNMENT;
+  if (blockmap_bytes < tree_blockmap_bytes(T_pad)) return TREE_ERR_WORKSPACE;
+  return cuda_result(tree::launch_blockmap_build(key_reach, T_pad, blockmap, dev_status, stream));
+}
+
+tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v,
+                            const int32_t* key_reach, const void* blockmap, int32_t T_pad,
+                            int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o,
+                            float* lse, int32_t* dev_status, tree_stream_t stream) {
+  tree_status_t st = check_attn_shape(T_pad, Hq, Hkv, d);
+  if (st != TREE_OK) return st;
+  if (!dev_status) return TREE_ERR_INVALID_ARG;
+  if (T_pad == 0) return TREE_OK;
+  if (!q || !k || !v || !key_reach || !blockmap || !o || !lse) return TREE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(key_reach) || !aligned16(blockmap))
+    return TREE_ERR_ALIGNMENT;
+  CUtensorMap tq, tk, tv;
+  if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
+      !encode_map(&tv, v, T_pad, Hkv, d))
+    return TREE_ERR_CUDA;
+  return cuda_result(tree::launch_attn_fwd(tq, tk, tv, key_reach, blockmap, T_pad, Hq, Hkv, d,
+                                           scale, o, lse, dev_status, stream));
+}
+
+size_t tree_attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d) {
+  if (T_pad < 0 || Hq <= 0 || d <= 0) return 0;
+  return tree::attn_bwd_workspace_bytes(T_pad, Hq, d);
+}
+
+tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                            const void* d_o, const float* lse, const int32_t* key_reach,
+                            const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
+                            int32_t d, float scale, void* dq, void* dk, void* dv,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            tree_stream_t stream) {
+  tree_status_t st = check_attn_shape(T_pad, Hq, Hkv, d);
+  if (st != TREE_OK) return st;
+  if (!dev_status) return TREE_ERR_INVALID_ARG;
+  if (T_pad == 0) return TREE_OK;
+  if (!q || !k || !v || !o || !d_o || !lse || !key_reach || !blockmap || !dq || !dk || !dv ||
+      !workspace)
+    return TREE_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, d_o, lse, key_reach, blockmap, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return TREE_ERR_ALIGNMENT;
+  if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
+      !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&tdo, d_o, T_pad, Hq, d))
+    return TREE_ERR_CUDA;
+  return cuda_result(tree::launch_attn_bwd(tq, tk, tv, tdo, o, d_o, lse, key_reach, blockmap,
+                                           T_pad, Hq, Hkv, d, scale, dq, dk, dv, workspace,
+                                           dev_status, stream, num_sms_current()));
+}
+
+}  // extern "C"

@@ -1,0 +1,462 @@
+// tree_attn_bwd: backward of the tree-masked attention on tcgen05/TMEM.
+//
+// AREAL-DTA, section 3 "Problem formalisation": the training loss is a sum of
+// per-sequence losses, a shared prefix is processed once, and its gradient
+// accumulates the contributions of all descendant sequences.  Here that is
+// automatic: a shared-prefix key is visible to the queries of every
+// continuation, so its dK/dV sum over all of them.
+//
+// Kernels:
+//  a4 prep     D[h,i] = sum_d dO[i,h,d] O[i,h,d];  lse2 = LSE * log2(e);
+//              the fp32 dQ accumulator is zeroed.
+//  a5 main     one CTA per (key block kb, kv head).  The key block's
+//              non-empty query tiles form the column run kb..col_hi of the
+//              blockmap; the CTA visits every (query head of this kv head,
+//              query block) pair of that run.  Per pair, with keys on TMEM
+//              lanes (M = 128 keys):
+//                S^T  = K Q^T            SS  -> TMEM [256,384)
+//                dP^T = V dO^T           SS  -> TMEM [384,512)
+//                P^T  = exp2(S^T*scale*log2e - lse2)  (mask on PARTIAL tiles)
+//                dS^T = P^T * (dP^T - D)
+//                dV  += P^T dO           TS (P^T bf16 in TMEM) -> [0, d)
+//                dK  += dS^T Q           TS (dS^T bf16 in TMEM) -> [128, 128+d)
+//                dQ   = dS K             SS (dS staged in smem, MN-major)
+//                                        -> TMEM [384, 384+d), then fp32
+//                                        vector atomics into the accumulator.
+//              warp 0: TMA producer (K, V once; Q, dO, lse2, D per pair in a
+//              2-stage ring); warp 1: TMEM allocator + MMA issuer; warps 2-5
+//              and 6-9: element-wise work on query columns 0-63 and 64-127.
+//  a6 convert  dQ = bf16(scale * accumulator).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace tree {
+namespace {
+
+constexpr int kBwdThreads = 320;
+
+template <int D>
+struct __align__(1024) BwdSmem {
+  __nv_bfloat16 k[kBlock * D];          // resident key tile (D/64 swizzled sub-tiles)
+  __nv_bfloat16 v[kBlock * D];
+  __nv_bfloat16 q[2][kBlock * D];       // ring stages
+  __nv_bfloat16 dout[2][kBlock * D];
+  __nv_bfloat16 ds[kBlock * kBlock];    // dS^T as [key][query], two 64-query halves
+  float lse2[2][kBlock];
+  float dd[2][kBlock];
+  uint64_t bar_kv;
+  uint64_t full[2], empty[2];
+  uint64_t s_full, dp_full, ew_done, dvdk_done, dq_full, dq_free, drain;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+struct BwdParams {
+  const int32_t* key_reach;
+  const int32_t* blockmap;
+  const float* lse2;          // [Hq, T_pad]
+  const float* dd;            // [Hq, T_pad]
+  float* dq_acc;              // [T_pad, Hq, D]
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int32_t T_pad, Hq, Hkv, nb;
+  float scale, scale_log2;
+  int32_t* status;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  if (ld_status(p.status)) return;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {          // the layout needs 1024-byte alignment
+    if (threadIdx.x == 0) set_status(p.status, TREE_ERR_UNSUPPORTED);
+    return;
+  }
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BlockmapView bm{p.nb, const_cast<int32_t*>(p.blockmap)};
+  const int32_t kb = bm.col_order()[blockIdx.x / p.Hkv];
+  const int32_t kvh = blockIdx.x % p.Hkv;
+  const int32_t g = p.Hq / p.Hkv;
+  const int32_t col_hi = bm.col_hi()[kb];
+  const int32_t col_full_hi = bm.col_full_hi()[kb];
+  const int32_t col_len = col_hi >= kb ? col_hi - kb + 1 : 0;
+  const int32_t nsteps = col_len * g;
+  AbortState ab{&sm.abort_flag, p.status};
+
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    mbar_init(&sm.bar_kv, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.ew_done, 256);
+    mbar_init(&sm.dvdk_done, 1);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_free, 256);
+    mbar_init(&sm.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_slot;
+  constexpr uint32_t kTileBytes = kBlock * D * 2;
+  constexpr int kHalves = D / 64;
+  constexpr uint32_t kDV = 0, kDK = 128, kS = 256, kDP = 384, kDQ = 384;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nsteps > 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_do);
+      mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTileBytes);
+      for (int hf = 0; hf < kHalves; ++hf) {
+        tma_load_3d(sm.k + hf * kBlock * 64, &tm_k, &sm.bar_kv, hf * 64, kvh, kb * kBlock);
+        tma_load_3d(sm.v + hf * kBlock * 64, &tm_v, &sm.bar_kv, hf * 64, kvh, kb * kBlock);
+      }
+      int issued = 0;
+      for (int n = 0; n < nsteps; ++n) {
+        const int s = n & 1;
+        if (n >= 2 && !mbar_wait(&sm.empty[s], ((n >> 1) - 1) & 1, ab)) break;
+        const int32_t h = kvh * g + n / col_len;
+        const int32_t qa = kb + n % col_len;
+        mbar_arrive_expect_tx(&sm.full[s], 2 * kTileBytes + 2 * kBlock * 4);
+        for (int hf = 0; hf < kHalves; ++hf) {
+          tma_load_3d(sm.q[s] + hf * kBlock * 64, &tm_q, &sm.full[s], hf * 64, h, qa * kBlock);
+          tma_load_3d(sm.dout[s] + hf * kBlock * 64, &tm_do, &sm.full[s], hf * 64, h, qa * kBlock);
+        }
+        const size_t row0 = static_cast<size_t>(h) * p.T_pad + qa * kBlock;
+        bulk_load(sm.lse2[s], p.lse2 + row0, kBlock * 4, &sm.full[s]);
+        bulk_load(sm.dd[s], p.dd + row0, kBlock * 4, &sm.full[s]);
+        issued = n + 1;
+      }
+      if (sm.abort_flag) {
+        mbar_drain(&sm.bar_kv, 0);
+        for (int n = (issued > 2 ? issued - 2 : 0); n < issued; ++n)
+          mbar_drain(&sm.full[n & 1], (n >> 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0 && nsteps > 0) {
+      constexpr uint32_t kIdescSS = idesc_bf16_f32(kBlock, kBlock, 0, 0);   // K-major both
+      constexpr uint32_t kIdescTS = idesc_bf16_f32(kBlock, D, 0, 1);        // B MN-major
+      constexpr uint32_t kIdescDQ = idesc_bf16_f32(kBlock, D, 1, 1);        // A, B MN-major
+      const uint32_t kbase = smem_u32(sm.k), vbase = smem_u32(sm.v), dsbase = smem_u32(sm.ds);
+      bool ok = mbar_wait(&sm.bar_kv, 0, ab);
+      for (int n = 0; ok && n < nsteps; ++n) {
+        const int s = n & 1;
+        if (!(ok = mbar_wait(&sm.full[s], (n >> 1) & 1, ab))) break;
+        tc_fence_after();
+        const uint32_t qbase = smem_u32(sm.q[s]), obase = smem_u32(sm.dout[s]);
+        if (n > 0) {
+          if (!(ok = mbar_wait(&sm.dvdk_done, (n - 1) & 1, ab))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kBlock * 128) + (kk & 3) * 32;
+          umma_ss(tbase + kS, sdesc_sw128(kbase + off, 16, 1024),
+                  sdesc_sw128(qbase + off, 16, 1024), kIdescSS, kk > 0);
+        }
+        umma_commit(&sm.s_full);
+        if (n > 0) {
+          if (!(ok = mbar_wait(&sm.dq_free, (n - 1) & 1, ab))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kBlock * 128) + (kk & 3) * 32;
+          umma_ss(tbase + kDP, sdesc_sw128(vbase + off, 16, 1024),
+                  sdesc_sw128(obase + off, 16, 1024), kIdescSS, kk > 0);
+        }
+        umma_commit(&sm.dp_full);
+        if (!(ok = mbar_wait(&sm.ew_done, n & 1, ab))) break;
+        tc_fence_after();
+        // P^T for queries 0-63 sits at [256,288), 64-127 at [320,352);
+        // dS^T at [288,320) and [352,384).
+#pragma unroll
+        for (int kk = 0; kk < kBlock / 16; ++kk) {
+          const uint32_t pcol = kS + (kk >> 2) * 64 + (kk & 3) * 8;
+          umma_ts(tbase + kDV, tbase + pcol, sdesc_sw128(obase + kk * 2048, kBlock * 128, 1024),
+                  kIdescTS, (n > 0 || kk > 0));
+        }
+#pragma unroll
+        for (int kk = 0; kk < kBlock / 16; ++kk) {
+          const uint32_t dcol = kS + 32 + (kk >> 2) * 64 + (kk & 3) * 8;
+          umma_ts(tbase + kDK, tbase + dcol, sdesc_sw128(qbase + kk * 2048, kBlock * 128, 1024),
+                  kIdescTS, (n > 0 || kk > 0));
+        }
+        umma_commit(&sm.dvdk_done);
+#pragma unroll
+        for (int kk = 0; kk < kBlock / 16; ++kk)
+          umma_ss(tbase + kDQ, sdesc_sw128(dsbase + kk * 2048, kBlock * 128, 1024),
+                  sdesc_sw128(kbase + kk * 2048, kBlock * 128, 1024), kIdescDQ, kk > 0);
+        umma_commit(&sm.dq_full);
+        umma_commit(&sm.empty[s]);
+      }
+      if (!ok) {
+        umma_commit(&sm.drain);
+        mbar_drain(&sm.drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------ element-wise warps
+    const int w = (warp - 2) >> 2;          // query half
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;      // key row (TMEM lane)
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int32_t jkey = kb * kBlock + r;
+    const int32_t reach = p.key_reach[jkey];
+    bool ok = true;
+    for (int n = 0; ok && n < nsteps; ++n) {
+      const int s = n & 1;
+      const int32_t h = kvh * g + n / col_len;
+      const int32_t qa = kb + n % col_len;
+      const bool partial = (qa == kb) || (qa > col_full_hi);
+      if (!(ok = mbar_wait_warp(&sm.s_full, n & 1, ab))) break;
+      tc_fence_after();
+      float pv[64];
+      {
+        uint32_t reg[32];
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          tmem_ld32(tbase + lane_off + kS + w * 64 + c2 * 32, reg);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pv[c2 * 32 + e] = __uint_as_float(reg[e]);
+        }
+      }
+      const float* lse2 = sm.lse2[s] + w * 64;
+      const int32_t q0 = qa * kBlock + w * 64;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const bool vis = !partial || (jkey <= q0 + c && q0 + c <= reach);
+        const float e = ex2(pv[c] * p.scale_log2 - lse2[c]);
+        pv[c] = vis ? e : 0.f;
+      }
+      if (!(ok = mbar_wait_warp(&sm.dp_full, n & 1, ab))) break;
+      tc_fence_after();
+      uint32_t pk[32], dsw[32];
+      {
+        const float* dd = sm.dd[s] + w * 64;
+        uint32_t reg[32];
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          tmem_ld32(tbase + lane_off + kDP + w * 64 + c2 * 32, reg);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = c2 * 32 + 2 * e;
+            const float ds0 = pv[c] * (__uint_as_float(reg[2 * e]) - dd[c]);
+            const float ds1 = pv[c + 1] * (__uint_as_float(reg[2 * e + 1]) - dd[c + 1]);
+            pk[c2 * 16 + e] = pack_bf16x2(pv[c], pv[c + 1]);
+            dsw[c2 * 16 + e] = pack_bf16x2(ds0, ds1);
+          }
+        }
+      }
+      tmem_st32(tbase + lane_off + kS + w * 64, pk);
+      tmem_st32(tbase + lane_off + kS + w * 64 + 32, dsw);
+      // dS^T row r, queries w*64 .. w*64+63 -> swizzled [key][query] half w.
+      {
+        uint8_t* row = reinterpret_cast<uint8_t*>(sm.ds) + w * (kBlock * 128) + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
+              make_uint4(dsw[4 * c], dsw[4 * c + 1], dsw[4 * c + 2], dsw[4 * c + 3]);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm.ew_done);
+      // dQ rows (TMEM lane = query row), columns w*D/2 .. of this head.
+      if (!(ok = mbar_wait_warp(&sm.dq_full, n & 1, ab))) break;
+      tc_fence_after();
+      float* dst = p.dq_acc + (static_cast<size_t>(qa * kBlock + r) * p.Hq + h) * D + w * (D / 2);
+#pragma unroll
+      for (int c2 = 0; c2 < D / 64; ++c2) {
+        uint32_t reg[32];
+        tmem_ld32(tbase + lane_off + kDQ + w * (D / 2) + c2 * 32, reg);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          atomicAdd(reinterpret_cast<float4*>(dst + c2 * 32 + 4 * e),
+                    make_float4(__uint_as_float(reg[4 * e]), __uint_as_float(reg[4 * e + 1]),
+                                __uint_as_float(reg[4 * e + 2]), __uint_as_float(reg[4 * e + 3])));
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.dq_free);
+    }
+    // ---------------------------------------------------------- epilogue
+    __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(jkey) * p.Hkv + kvh) * D + w * (D / 2);
+    __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(jkey) * p.Hkv + kvh) * D + w * (D / 2);
+    if (ok && nsteps > 0 && mbar_wait_warp(&sm.dvdk_done, (nsteps - 1) & 1, ab)) {
+      tc_fence_after();
+#pragma unroll
+      for (int c2 = 0; c2 < D / 64; ++c2) {
+        uint32_t rv[32], rk[32];
+        tmem_ld32(tbase + lane_off + kDV + w * (D / 2) + c2 * 32, rv);
+        tmem_ld32(tbase + lane_off + kDK + w * (D / 2) + c2 * 32, rk);
+#pragma unroll
+        for (int e8 = 0; e8 < 4; ++e8) {
+          uint4 a, b;
+          const float* fv = reinterpret_cast<const float*>(rv + e8 * 8);
+          const float* fk = reinterpret_cast<const float*>(rk + e8 * 8);
+          a = make_uint4(pack_bf16x2(fv[0], fv[1]), pack_bf16x2(fv[2], fv[3]),
+                         pack_bf16x2(fv[4], fv[5]), pack_bf16x2(fv[6], fv[7]));
+          b = make_uint4(pack_bf16x2(fk[0] * p.scale, fk[1] * p.scale),
+                         pack_bf16x2(fk[2] * p.scale, fk[3] * p.scale),
+                         pack_bf16x2(fk[4] * p.scale, fk[5] * p.scale),
+                         pack_bf16x2(fk[6] * p.scale, fk[7] * p.scale));
+          *reinterpret_cast<uint4*>(dvrow + c2 * 32 + e8 * 8) = a;
+          *reinterpret_cast<uint4*>(dkrow + c2 * 32 + e8 * 8) = b;
+        }
+      }
+    } else if (nsteps == 0) {
+#pragma unroll
+      for (int c = 0; c < D / 2; c += 8) {
+        *reinterpret_cast<uint4*>(dvrow + c) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(dkrow + c) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// a4: D rows, lse2 rows, zeroed dQ accumulator.  One warp per (token, head).
+template <int D>
+__global__ void __launch_bounds__(256)
+tree_attn_bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse,
+                          float* dd, float* lse2, float* dq_acc, int32_t T_pad, int32_t Hq,
+                          const int32_t* status) {
+  if (ld_status(status)) return;
+  const int64_t rows = static_cast<int64_t>(T_pad) * Hq;
+  const int lane = threadIdx.x & 31;
+  for (int64_t row = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; row < rows;
+       row += (int64_t(gridDim.x) * blockDim.x) >> 5) {
+    const int64_t i = row / Hq, h = row % Hq;
+    constexpr int kPer = D / 32;     // elements per lane (2 or 4)
+    float acc = 0.f;
+    const __nv_bfloat16* po = o + row * D + lane * kPer;
+    const __nv_bfloat16* pd = dout + row * D + lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(po + e));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(pd + e));
+      acc += a.x * b.x + a.y * b.y;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    float4* z = reinterpret_cast<float4*>(dq_acc + row * D);
+    for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) {
+      dd[h * T_pad + i] = acc;
+      lse2[h * T_pad + i] = lse[h * T_pad + i] * 1.4426950408889634f;
+    }
+  }
+}
+
+// a6: dQ = bf16(scale * acc), 8 elements per thread.
+__global__ void __launch_bounds__(256)
+tree_attn_bwd_dq_kernel(const float* dq_acc, __nv_bfloat16* dq, int64_t n8, float scale,
+                        const int32_t* status) {
+  if (ld_status(status)) return;
+  for (int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; t < n8;
+       t += int64_t(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * t];
+    const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * t + 1];
+    reinterpret_cast<uint4*>(dq)[t] =
+        make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                   pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const void* o, const void* d_o,
+                         const float* lse, BwdParams p, void* dq, float* lse2_ws, float* dd_ws,
+                         cudaStream_t s, int num_sms) {
+  const int64_t rows = static_cast<int64_t>(p.T_pad) * p.Hq;
+  int prep_blocks = static_cast<int>((rows * 32 + 255) / 256);
+  if (prep_blocks > num_sms * 16) prep_blocks = num_sms * 16;
+  tree_attn_bwd_prep_kernel<D><<<prep_blocks, 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, dd_ws,
+      lse2_ws, p.dq_acc, p.T_pad, p.Hq, p.status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(BwdSmem<D>);
+  e = cudaFuncSetAttribute(tree_attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  tree_attn_bwd_kernel<D><<<p.nb * p.Hkv, kBwdThreads, smem, s>>>(tq, tk, tv, tdo, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t n8 = rows * D / 8;
+  int cv_blocks = static_cast<int>((n8 + 255) / 256);
+  if (cv_blocks > num_sms * 16) cv_blocks = num_sms * 16;
+  tree_attn_bwd_dq_kernel<<<cv_blocks, 256, 0, s>>>(p.dq_acc, static_cast<__nv_bfloat16*>(dq),
+                                                   n8, p.scale, p.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d) {
+  const size_t rows = static_cast<size_t>(T_pad) * Hq;
+  return rows * d * sizeof(float) + 2 * rows * sizeof(float);
+}
+
+cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const void* o, const void* d_o,
+                            const float* lse, const int32_t* key_reach, const void* blockmap,
+                            int32_t T_pad, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                            void* dq, void* dk, void* dv, void* workspace, int32_t* status,
+                            cudaStream_t s, int num_sms) {
+  const size_t rows = static_cast<size_t>(T_pad) * Hq;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* dd_ws = dq_acc + rows * d;
+  float* lse2_ws = dd_ws + rows;
+  BwdParams p;
+  p.key_reach = key_reach;
+  p.blockmap = static_cast<const int32_t*>(blockmap);
+  p.lse2 = lse2_ws;
+  p.dd = dd_ws;
+  p.dq_acc = dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.T_pad = T_pad;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.nb = T_pad / kBlock;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = status;
+  return d == 64 ? launch_bwd_d<64>(tq, tk, tv, tdo, o, d_o, lse, p, dq, lse2_ws, dd_ws, s, num_sms)
+                 : launch_bwd_d<128>(tq, tk, tv, tdo, o, d_o, lse, p, dq, lse2_ws, dd_ws, s, num_sms);
+}
+
+}  // namespace tree

@@ -1,0 +1,333 @@
+// tree_attn_fwd: tree-masked flash attention forward on tcgen05/TMEM.
+//
+// AReaL Tree Training guide, packing figure and section "两种注意力实现":
+// softmax attention under the ancestor mask, consumed in 128-token blocks,
+// batch 1.  Visibility is the interval test j <= i <= key_reach[j]; EMPTY
+// tiles never reach the kernel (the blockmap lists only non-empty ones) and
+// the per-element test runs only on PARTIAL tiles.
+//
+// One CTA = one 128-row query block x up to two query heads that read the
+// same key/value head (GQA), so each K/V tile is loaded once for both.
+//   warp 0     TMA producer: Q tiles once, then K, V (and the 128 reach
+//              values) per listed key block through a 2-stage ring.
+//   warp 1     TMEM allocator and MMA issuer (one thread):
+//                S_t = Q_t K^T   (SS, both K-major)          -> TMEM S_t
+//                O_t += P_t V    (TS: P_t read from TMEM, V MN-major)
+//   warps 2-5  softmax for head slot 0, warps 6-9 for head slot 1.  One
+//              thread owns one query row (TMEM lane), so row max and row sum
+//              need no shuffles.  P is written back as bf16 over the first
+//              64 columns of S_t and consumed there by the PV MMA.
+// TMEM: S_0 [0,128) S_1 [128,256) O_0 [256,256+d) O_1 [384,384+d).
+// The issuer starts QK of tile k+1 for a head slot only after PV of tile k
+// for that slot has completed, so P/S aliasing is safe and the O rescale in
+// the softmax warps never races an MMA; the two slots interleave on the
+// tensor pipe.  The running max is refreshed only when it grows by more than
+// 8 (log2 units): P stays <= 256, and O is rescaled in TMEM only then.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace tree {
+namespace {
+
+constexpr int kFwdThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct __align__(1024) FwdSmem {
+  __nv_bfloat16 q[2][kBlock * D];      // per head slot, D/64 swizzled [128][64] sub-tiles
+  __nv_bfloat16 k[2][kBlock * D];      // ring stages
+  __nv_bfloat16 v[2][kBlock * D];
+  int32_t reach[2][kBlock];
+  uint64_t bar_q;
+  uint64_t kv_full[2], kv_empty[2];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t drain;
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+struct FwdParams {
+  const int32_t* key_reach;
+  const int32_t* blockmap;
+  int32_t T_pad, Hq, Hkv, nb, heads_per_cta, n_hgroups;
+  float scale_log2;                    // softmax scale * log2(e)
+  __nv_bfloat16* o;
+  float* lse;
+  int32_t* status;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  if (ld_status(p.status)) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* aligned = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(aligned);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BlockmapView bm{p.nb, const_cast<int32_t*>(p.blockmap)};
+  const int32_t qa = bm.row_order()[blockIdx.x / p.n_hgroups];
+  const int32_t h0 = (blockIdx.x % p.n_hgroups) * p.heads_per_cta;
+  const int nh = p.heads_per_cta;
+  const int32_t kvh = h0 / (p.Hq / p.Hkv);
+  const int32_t ntiles = bm.row_cnt()[qa];
+  const int32_t nfull = bm.row_nfull()[qa];
+  const int32_t* tiles = bm.row_idx() + bm.row_ptr()[qa];
+  AbortState ab{&sm.abort_flag, p.status};
+
+  if (threadIdx.x == 0) {
+    sm.abort_flag = 0;
+    mbar_init(&sm.bar_q, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.p_full[s], kBlock);
+      mbar_init(&sm.o_full[s], 1);
+    }
+    mbar_init(&sm.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_slot;
+  constexpr uint32_t kTileBytes = kBlock * D * 2;
+  constexpr int kHalves = D / 64;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && ntiles > 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      mbar_arrive_expect_tx(&sm.bar_q, nh * kTileBytes);
+      for (int t = 0; t < nh; ++t)
+        for (int hf = 0; hf < kHalves; ++hf)
+          tma_load_3d(sm.q[t] + hf * kBlock * 64, &tm_q, &sm.bar_q, hf * 64, h0 + t, qa * kBlock);
+      int issued = 0;
+      for (int k = 0; k < ntiles; ++k) {
+        const int s = k & 1;
+        if (k >= 2 && !mbar_wait(&sm.kv_empty[s], ((k >> 1) - 1) & 1, ab)) break;
+        const int32_t kb = tiles[k];
+        mbar_arrive_expect_tx(&sm.kv_full[s], 2 * kTileBytes + kBlock * 4);
+        for (int hf = 0; hf < kHalves; ++hf) {
+          tma_load_3d(sm.k[s] + hf * kBlock * 64, &tm_k, &sm.kv_full[s], hf * 64, kvh, kb * kBlock);
+          tma_load_3d(sm.v[s] + hf * kBlock * 64, &tm_v, &sm.kv_full[s], hf * 64, kvh, kb * kBlock);
+        }
+        bulk_load(sm.reach[s], p.key_reach + kb * kBlock, kBlock * 4, &sm.kv_full[s]);
+        issued = k + 1;
+      }
+      if (sm.abort_flag) {
+        // Let every copy already issued land before the CTA can exit.
+        mbar_drain(&sm.bar_q, 0);
+        for (int k = (issued > 2 ? issued - 2 : 0); k < issued; ++k)
+          mbar_drain(&sm.kv_full[k & 1], (k >> 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlock, kBlock, 0, 0);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlock, D, 0, 1);
+      bool ok = mbar_wait(&sm.bar_q, 0, ab);
+      for (int k = 0; ok && k < ntiles; ++k) {
+        const int s = k & 1;
+        if (!(ok = mbar_wait(&sm.kv_full[s], (k >> 1) & 1, ab))) break;
+        tc_fence_after();
+        const uint32_t kbase = smem_u32(sm.k[s]);
+        for (int t = 0; t < nh && ok; ++t) {
+          if (k > 0) {
+            if (!(ok = mbar_wait(&sm.o_full[t], (k - 1) & 1, ab))) break;
+            tc_fence_after();
+          }
+          const uint32_t qbase = smem_u32(sm.q[t]);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (kBlock * 128) + (kk & 3) * 32;
+            umma_ss(tbase + t * 128, sdesc_sw128(qbase + off, 16, 1024),
+                    sdesc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0);
+          }
+          umma_commit(&sm.s_full[t]);
+        }
+        const uint32_t vbase = smem_u32(sm.v[s]);
+        for (int t = 0; t < nh && ok; ++t) {
+          if (!(ok = mbar_wait(&sm.p_full[t], k & 1, ab))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBlock / 16; ++kk)
+            umma_ts(tbase + 256 + t * 128, tbase + t * 128 + kk * 8,
+                    sdesc_sw128(vbase + kk * 2048, kBlock * 128, 1024), kIdescPV,
+                    (k > 0 || kk > 0));
+          umma_commit(&sm.o_full[t]);
+        }
+        if (ok) umma_commit(&sm.kv_empty[s]);
+      }
+      if (!ok) {
+        umma_commit(&sm.drain);   // wait for every MMA already issued
+        mbar_drain(&sm.drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    if (t < nh) {
+      const int32_t h = h0 + t;
+      const int32_t i = qa * kBlock + r;
+      const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t s_addr = tbase + lane_off + t * 128;
+      const uint32_t o_addr = tbase + lane_off + 256 + t * 128;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int k = 0; k < ntiles; ++k) {
+        if (!(ok = mbar_wait_warp(&sm.s_full[t], k & 1, ab))) break;
+        tc_fence_after();
+        float x[kBlock];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t reg[32];
+          tmem_ld32(s_addr + c4 * 32, reg);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[c4 * 32 + e] = __uint_as_float(reg[e]);
+        }
+        if (k >= nfull) {
+          const int32_t* rch = sm.reach[k & 1];
+          const int32_t j0 = tiles[k] * kBlock;
+#pragma unroll
+          for (int c = 0; c < kBlock; ++c) {
+            const bool vis = (j0 + c <= i) && (i <= rch[c]);
+            x[c] = vis ? x[c] * p.scale_log2 : -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBlock; ++c) x[c] *= p.scale_log2;
+        }
+        float mt = x[0];
+#pragma unroll
+        for (int c = 1; c < kBlock; ++c) mt = fmaxf(mt, x[c]);
+        const float mnew = fmaxf(m, mt);
+        if (mnew > m + kRescaleThreshold) {
+          const float alpha = ex2(m - mnew);   // 0 when m = -inf
+          if (k > 0) {
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+              uint32_t reg[32];
+              tmem_ld32(o_addr + c4 * 32, reg);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                reg[e] = __float_as_uint(__uint_as_float(reg[e]) * alpha);
+              tmem_st32(o_addr + c4 * 32, reg);
+            }
+          }
+          l *= alpha;
+          m = mnew;
+        }
+        const float msub = (m == -INFINITY) ? 0.f : m;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float p0 = ex2(x[c2 * 64 + 2 * e] - msub);
+            const float p1 = ex2(x[c2 * 64 + 2 * e + 1] - msub);
+            l += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(s_addr + c2 * 32, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[t]);
+      }
+      // ---------------------------------------------------------- epilogue
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(i) * p.Hq + h) * D;
+      if (ok && ntiles > 0 && mbar_wait_warp(&sm.o_full[t], (ntiles - 1) & 1, ab)) {
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t reg[32];
+          tmem_ld32(o_addr + c4 * 32, reg);
+#pragma unroll
+          for (int e8 = 0; e8 < 4; ++e8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 0]) * inv_l, __uint_as_float(reg[e8 * 8 + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 2]) * inv_l, __uint_as_float(reg[e8 * 8 + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 4]) * inv_l, __uint_as_float(reg[e8 * 8 + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 6]) * inv_l, __uint_as_float(reg[e8 * 8 + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + c4 * 32 + e8 * 8) = w;
+          }
+        }
+        p.lse[static_cast<size_t>(h) * p.T_pad + i] =
+            l > 0.f ? m * 0.69314718055994531f + logf(l) : -INFINITY;
+      } else if (ntiles == 0) {
+#pragma unroll
+        for (int c = 0; c < D; c += 8)
+          *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
+        p.lse[static_cast<size_t>(h) * p.T_pad + i] = -INFINITY;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdParams& p, int grid, cudaStream_t s) {
+  const size_t smem = sizeof(FwdSmem<D>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(tree_attn_fwd_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  tree_attn_fwd_kernel<D><<<grid, kFwdThreads, smem, s>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const int32_t* key_reach, const void* blockmap, int32_t T_pad,
+                            int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o, float* lse,
+                            int32_t* status, cudaStream_t s) {
+  const int g = Hq / Hkv;
+  FwdParams p;
+  p.key_reach = key_reach;
+  p.blockmap = static_cast<const int32_t*>(blockmap);
+  p.T_pad = T_pad;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.nb = T_pad / kBlock;
+  p.heads_per_cta = (g % 2 == 0) ? 2 : 1;
+  p.n_hgroups = Hq / p.heads_per_cta;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.status = status;
+  const int grid = p.nb * p.n_hgroups;
+  return d == 64 ? launch_fwd_d<64>(tq, tk, tv, p, grid, s)
+                 : launch_fwd_d<128>(tq, tk, tv, p, grid, s);
+}
+
+}  // namespace tree

@@ -1,0 +1,523 @@
+"""Benchmark of the packed-trie attention hot path on GB300.
+
+One step = the whole hot path over one batch of the workload: for every trie
+of the batch, position ids + key reach (a1), blockmap (a2), attention forward
+(a3), backward prepare / main / finish (a4-a6).  Default workload: GRPO-style
+groups (64 prompts x 8 responses, first-fit-decreasing into 32768-token tries,
+Qwen3-8B attention heads 32 q / 8 kv, head_dim 128), seeded synthetic data.
+
+Metric: effective TFLOP/s = 14 * d * Hq * (visible pairs) / step time, where
+visible pairs count only unmasked (i, j) over real tokens (4 d Hq per pair
+for the forward, 10 d Hq for the backward).  Packed tokens/s is reported too.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own batch (seed = rank): weak scaling, no
+collective on the data path; rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "tree-attn fwd+bwd effective TFLOP/s and packed tokens/s vs bf16 TC peak"
+UNIT = "TFLOP/s"
+FWD_FLOPS_PER_PAIR = 4      # times d * Hq
+BWD_FLOPS_PER_PAIR = 10
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "bwd_main_traffic.json")
+KERNEL_SOURCE = os.path.join(ROOT, "prefix_tree_attention_gb300", "csrc", "attn_bwd.cu")
+
+
+# ------------------------------------------------------------------ helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(bf16=p["bf16_tflops"], bf16_sustained=p["bf16_tflops_sustained"],
+                    hbm=p["hbm_gbs"], source="measured")
+    return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+def source_hash(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the bwd main kernel from a committed ncu
+    summary, or None when absent or taken on a different kernel source."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_sha256_16") != source_hash(KERNEL_SOURCE):
+        return None
+    return rec.get("bytes_per_launch_full_workload")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_index: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v for v in vis.split(",") if v.strip()]
+        self.index = ids[local_index] if local_index < len(ids) else str(local_index)
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4)
+                          if s[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.samples)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle leg
+def oracle_sample(key: str, seed: int, budget_s: float, tensors_fn=None):
+    """Time the oracle (as it stands) on a bounded sample of the workload: the
+    per-row forward + backward of evenly spaced rows of the first trie, for
+    the query heads of key/value head 0.  Returns (TFLOP/s, description,
+    seconds, threads)."""
+    from oracle import attention as OA
+    from oracle import trie as OT
+    import torch
+
+    wl = W.WORKLOADS[key]
+    seqs = W.sequences(key, seed)
+    (ref, *_rest) = OT.pack_sequences(seqs, wl.max_tokens_per_mb)
+    g = wl.Hq // wl.Hkv
+    if tensors_fn is None:
+        t = W.tensors(ref.T_pad, wl.Hq, wl.Hkv, wl.d, seed=seed * 1000, device="cpu")
+    else:
+        t = tensors_fn(ref)
+    q = t["q"][:, :g].double().numpy()
+    k = t["k"][:, :1].double().numpy()
+    v = t["v"][:, :1].double().numpy()
+    do = t["do"][:, :g].double().numpy()
+    real = np.nonzero(ref.token_node >= 0)[0]
+    order = real[np.argsort((real * 0.6180339887) % 1.0)]   # spread-out row order
+    from oracle import mask as OM
+    done = []
+    t0 = time.perf_counter()
+    for i in order:
+        _o, _l, _dq, _dk, _dv = OA.rows_forward_backward(q, k, v, do, ref, [int(i)], range(g))
+        done.append(int(i))
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    rows_done = len(done)
+    pairs = sum(int(OM.mask_rows(ref, i, i + 1).sum()) for i in done)
+    flops = (FWD_FLOPS_PER_PAIR + BWD_FLOPS_PER_PAIR) * wl.d * g * pairs
+    desc = (f"oracle per-row fwd+bwd (fp64 numpy), {rows_done} rows of trie 0 of '{key}' "
+            f"({pairs} visible pairs), query heads 0-{g - 1} of kv head 0")
+    return flops / dt / 1e12, desc, dt, torch.get_num_threads()
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    vals = []
+    desc = cores = None
+    for step in range(args.warmup + args.steps):
+        v, desc, _dt, cores = oracle_sample(args.workload, args.seed, budget)
+        if step >= args.warmup:
+            vals.append(v)
+    value = float(np.median(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "description": W.WORKLOADS[args.workload].description},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+class TrieCase:
+    """Device-resident inputs, outputs and buffers of one trie."""
+
+    def __init__(self, ptg, tr, wl, seed, idx, device):
+        import torch
+        self.tr = tr
+        T = tr.T_pad
+        self.T, self.Hq, self.Hkv, self.d = T, wl.Hq, wl.Hkv, wl.d
+        self.token_node = torch.from_numpy(tr.token_node).to(device)
+        self.entry = torch.from_numpy(tr.node_entry).to(device)
+        self.exit = torch.from_numpy(tr.node_exit).to(device)
+        t = W.tensors(T, wl.Hq, wl.Hkv, wl.d, seed=seed * 1000 + idx, device=device)
+        self.q, self.k, self.v, self.do = t["q"], t["k"], t["v"], t["do"]
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((wl.Hq, T), dtype=torch.float32, device=device)
+        self.dq = torch.empty_like(self.q)
+        self.dk = torch.empty_like(self.k)
+        self.dv = torch.empty_like(self.v)
+        self.bufs = ptg.TrieBuffers(T, tr.n_nodes, wl.Hq, wl.d, device=device)
+        self.pairs = tr.visible_pairs
+        self.n_tokens = tr.n_tokens
+
+    def input_tensors(self):
+        return [self.token_node, self.entry, self.exit, self.q, self.k, self.v, self.do]
+
+    def output_tensors(self):
+        return [self.o, self.dq, self.dk, self.dv]
+
+
+def run_path(ptg, c, ws_bwd, stream, ev=None):
+    """Queue the whole hot path for one trie on `stream`."""
+    b = c.bufs
+    ptg.tree_pack_positions(c.token_node, c.entry, c.exit, b.position_ids, b.key_reach, b.pos_ws,
+                            b.status, stream=stream)
+    ptg.tree_blockmap_build(b.key_reach, b.blockmap, b.status, stream=stream)
+    if ev is not None:
+        ev[0].record(stream)
+    ptg.tree_attn_fwd(c.q, c.k, c.v, b.key_reach, b.blockmap, c.o, c.lse, b.status, stream=stream)
+    if ev is not None:
+        ev[1].record(stream)
+    ptg.tree_attn_bwd_prepare(c.o, c.do, c.lse, ws_bwd, b.status, stream=stream)
+    if ev is not None:
+        ev[2].record(stream)
+    ptg.tree_attn_bwd_main(c.q, c.k, c.v, c.do, b.key_reach, b.blockmap, c.dk, c.dv, ws_bwd,
+                           b.status, stream=stream)
+    if ev is not None:
+        ev[3].record(stream)
+    ptg.tree_attn_bwd_finish(ws_bwd, c.dq, b.status, stream=stream)
+
+
+def run_ours(args, rank, ws):
+    import torch
+    import prefix_tree_attention_gb300 as ptg
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    wl = W.WORKLOADS[args.workload]
+    seed = args.seed + rank
+    seqs = W.sequences(args.workload, seed)
+    tries = ptg.pack_sequences(seqs, wl.max_tokens_per_mb)
+    if args.tries:
+        tries = tries[:args.tries]
+        used = {s for tr in tries for s in tr.seq_ids}
+        seqs = [s for i, s in enumerate(seqs) if i in used]
+    cases = [TrieCase(ptg, tr, wl, seed, i, device) for i, tr in enumerate(tries)]
+    ws_bytes = max(ptg.attn_bwd_workspace_bytes(c.T, wl.Hq, wl.d) for c in cases)
+    ws_bwd = torch.empty((ws_bytes + 3) // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device=device)
+    pairs = sum(c.pairs for c in cases)
+    tokens = sum(c.n_tokens for c in cases)
+    original = sum(len(s) for s in seqs)
+    causal_pairs = sum(len(s) * (len(s) + 1) // 2 for s in seqs)
+    flops = (FWD_FLOPS_PER_PAIR + BWD_FLOPS_PER_PAIR) * wl.d * wl.Hq * pairs
+    bwd_flops = BWD_FLOPS_PER_PAIR * wl.d * wl.Hq * pairs
+    fwd_flops = FWD_FLOPS_PER_PAIR * wl.d * wl.Hq * pairs
+
+    def step(ev_list=None):
+        with torch.cuda.stream(stream):
+            for i, c in enumerate(cases):
+                run_path(ptg, c, ws_bwd, stream, None if ev_list is None else ev_list[i])
+
+    # ---- warm-up (also checks that nothing failed)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bad = [int(c.bufs.status.item()) for c in cases if int(c.bufs.status.item()) != 0]
+    if bad:
+        raise RuntimeError(f"device status {ptg.status_string(bad[0])} during warm-up")
+
+    # ---- device-resident timed region
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    per_step = []
+    launches0 = ptg.launch_count()
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            evs = [[mk() for _ in range(4)] for _ in cases]
+            s0, s1 = mk(), mk()
+            s0.record(stream)
+            step(evs)
+            s1.record(stream)
+            per_step.append((s0, s1, evs))
+        torch.cuda.synchronize()
+    barrier(ws)
+    launches = ptg.launch_count() - launches0
+    fwd_ms = sum(ev[0].elapsed_time(ev[1]) for _, _, evs in per_step for ev in evs)
+    bwd_main_ms = sum(ev[2].elapsed_time(ev[3]) for _, _, evs in per_step for ev in evs)
+    step_ms = [a.elapsed_time(b) for a, b, _ in per_step]
+    ms_per_step = float(np.mean(step_ms))
+    ms_max = max_over_ranks(ms_per_step, ws)
+    flops_all = sum_over_ranks(flops, ws)
+    value = flops_all / (ms_max * 1e-3) / 1e12
+    tokens_all = sum_over_ranks(tokens, ws)
+    statuses = [int(c.bufs.status.item()) for c in cases]
+    if any(statuses):
+        raise RuntimeError("device status " + ptg.status_string(max(statuses)))
+
+    # ---- roofline of the dominant kernel (bwd main) from the live events
+    peaks = measured_peaks()
+    n_launch = len(cases) * args.steps
+    bwd_achieved = bwd_flops * args.steps / (bwd_main_ms * 1e-3) / 1e12
+    fwd_achieved = fwd_flops * args.steps / (fwd_ms * 1e-3) / 1e12
+    traffic = recorded_traffic()
+    roofline = {
+        "kernel": "tree_attn_bwd_kernel (a5, bwd main)",
+        "bound": "tensor", "achieved": round(bwd_achieved, 1),
+        "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+        "frac": round(bwd_achieved / peaks["bf16_sustained"], 4),
+        "peak_kind": f"bf16 dense, sustained ({peaks['source']})",
+        "traffic": None if traffic is None else traffic / len(cases),
+        "avg_launch_ms": round(bwd_main_ms / n_launch, 4),
+        "flops_per_launch": bwd_flops / len(cases),
+        "fwd_achieved": round(fwd_achieved, 1),
+        "fwd_frac": round(fwd_achieved / peaks["bf16_sustained"], 4),
+    }
+
+    # ---- end to end through the API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(ptg, cases, ws_bwd, stream, args, ws, flops_all)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": args.workload + (f" (first {args.tries} tries)" if args.tries else ""),
+            "description": wl.description,
+            "tries": len(cases), "packed_tokens": tokens, "original_tokens": original,
+            "tree_token_ratio": round(tokens / original, 4),
+            "visible_pairs": pairs,
+            "flops_saved_vs_unpacked_causal": round(1 - pairs / causal_pairs, 4),
+            "heads": f"{wl.Hq}q/{wl.Hkv}kv", "head_dim": wl.d,
+            "packed_tokens_per_s": round(tokens_all / (ms_max * 1e-3), 1),
+            "fwd_ms_per_step": round(fwd_ms / args.steps, 3),
+            "bwd_main_ms_per_step": round(bwd_main_ms / args.steps, 3),
+            "l2": "inputs larger than L2 (no flush needed)",
+            "parallelism": f"replicas x{ws}",
+        },
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, desc, _dt, cores = oracle_sample(args.workload, args.seed, args.cpu_budget,
+                                            tensors_fn=None)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(ptg, cases, ws_bwd, stream, args, ws, flops_all):
+    """Same metric, each step copying its inputs host->device from pinned
+    memory and its outputs (O, dQ, dK, dV) device->host, through the same
+    API calls; copies overlap compute on a second stream."""
+    import torch
+    # Pinned host copies of every input and output.  Keep them well inside the
+    # host's available memory: if the whole batch does not fit in 40% of it,
+    # run the e2e leg on the leading tries that do and report that.
+    need = [sum(t.numel() * t.element_size() for t in c.input_tensors() + c.output_tensors())
+            for c in cases]
+    avail = _mem_available_bytes()
+    budget = 0.4 * avail if avail else float(sum(need))
+    n_fit, acc = 0, 0
+    for b in need:
+        if acc + b > budget:
+            break
+        acc += b
+        n_fit += 1
+    if n_fit == 0:
+        return {"value": None, "unit": UNIT, "skipped": "host memory too small for pinned buffers"}
+    subset = n_fit < len(cases)
+    cases = cases[:n_fit]
+    if subset:
+        flops_all = sum_over_ranks(
+            (FWD_FLOPS_PER_PAIR + BWD_FLOPS_PER_PAIR) * cases[0].d * cases[0].Hq *
+            sum(c.pairs for c in cases), ws)
+    host_in = [[t.cpu().pin_memory() for t in c.input_tensors()] for c in cases]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in c.output_tensors()]
+                for c in cases]
+    h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
+    d2h = sum(t.numel() * t.element_size() for hs in host_out for t in hs)
+    copy_in = torch.cuda.Stream()
+    copy_out = torch.cuda.Stream()
+
+    def e2e_step():
+        # outputs of the previous step must be downloaded before they are rewritten
+        stream.wait_stream(copy_out)
+        ready = []
+        for i, c in enumerate(cases):
+            with torch.cuda.stream(copy_in):
+                for dst, src in zip(c.input_tensors(), host_in[i]):
+                    dst.copy_(src, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_in)
+            ready.append(ev)
+        done = []
+        for i, c in enumerate(cases):
+            stream.wait_event(ready[i])
+            with torch.cuda.stream(stream):
+                run_path(ptg, c, ws_bwd, stream)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+            done.append(ev)
+            copy_out.wait_event(ev)
+            with torch.cuda.stream(copy_out):
+                for dst, src in zip(host_out[i], c.output_tensors()):
+                    dst.copy_(src, non_blocking=True)
+        # the next step's uploads must not overwrite inputs still in use
+        copy_in.wait_stream(stream)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / args.steps
+    dt = max_over_ranks(dt, ws)
+    rec = {"value": round(flops_all / dt / 1e12, 2), "unit": UNIT,
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+           "ms_per_step": round(dt * 1e3, 3),
+           "copies": "pinned host -> device inputs (token_node, entry, exit, q, k, v, do); "
+                     "device -> pinned host outputs (o, dq, dk, dv); copy streams overlap compute"}
+    if subset:
+        rec["tries"] = f"first {len(cases)} tries (pinned buffers limited to 40% of host memory)"
+    return rec
+
+
+def _mem_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="grpo", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--tries", type=int, default=0,
+                    help="use only the first N tries of the batch (small profiling cases)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank, ws = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, ws)
+    else:
+        run_ours(args, rank, ws)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

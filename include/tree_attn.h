@@ -206,6 +206,30 @@ TREE_API tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v
                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
                             tree_stream_t stream);
 
+/* The three steps of tree_attn_bwd, callable one by one on the same stream
+ * (tree_attn_bwd is exactly prepare, main, finish):
+ *   prepare  D[h,i] = sum_d dO[i,h,d] O[i,h,d] and LSE*log2(e) into the
+ *            workspace; zero the fp32 dQ accumulator.       (HBM-bound)
+ *   main     recompute S and P per non-empty tile, dS = P*(dP - D), dK and
+ *            dV into dk/dv (bf16, dK scaled), dS K added into the fp32 dQ
+ *            accumulator (tensor cores; the dominant step)
+ *   finish   dq = bf16(scale * accumulator)                 (HBM-bound)
+ * Arguments as for tree_attn_bwd; the workspace must be the same buffer for
+ * all three. */
+TREE_API tree_status_t tree_attn_bwd_prepare(const void* o, const void* d_o, const float* lse,
+                                             int32_t T_pad, int32_t Hq, int32_t d,
+                                             void* workspace, size_t workspace_bytes,
+                                             int32_t* dev_status, tree_stream_t stream);
+TREE_API tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v,
+                                          const void* d_o, const int32_t* key_reach,
+                                          const void* blockmap, int32_t T_pad, int32_t Hq,
+                                          int32_t Hkv, int32_t d, float scale, void* dk, void* dv,
+                                          void* workspace, size_t workspace_bytes,
+                                          int32_t* dev_status, tree_stream_t stream);
+TREE_API tree_status_t tree_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
+                                            const void* workspace, size_t workspace_bytes,
+                                            void* dq, int32_t* dev_status, tree_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Host packer: sequences -> tries in the layout above.
  *
@@ -265,6 +289,10 @@ TREE_API tree_status_t tree_packing_seq_indices(const tree_packing_t* packing, i
  * ---------------------------------------------------------------------- */
 TREE_API tree_status_t tree_debug_wait_timeout(int32_t* dev_status, int64_t limit_ns,
                                                tree_stream_t stream);
+
+/* tree_launch_count — number of kernels the library has queued in this
+ * process, over all entry points (for launch accounting in benchmarks). */
+TREE_API uint64_t tree_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -152,15 +152,26 @@ def key_grads(q, k, v, do, packed, keys, kv_heads, scale=None):
     dk, dv = {}, {}
     for j in keys:
         rows = rows_seeing_key(packed, j)
+        row_keys = {int(i): np.nonzero(mask_rows(packed, int(i), int(i) + 1)[0])[0]
+                    for i in rows}
         for kv in kv_heads:
             acc_k = np.zeros(d)
             acc_v = np.zeros(d)
-            heads = range(kv * g, (kv + 1) * g)
-            o, lse, dq, dk_part, dv_part = rows_forward_backward(
-                q, k, v, do, packed, rows, heads, scale)
-            if kv in dk_part:
-                acc_k = dk_part[kv][j]
-                acc_v = dv_part[kv][j]
+            for h in range(kv * g, (kv + 1) * g):
+                for i in rows:
+                    # row i's softmax over its own keys, then key j's share
+                    ks = row_keys[int(i)]
+                    kk = k[ks, kv, :]
+                    vv = v[ks, kv, :]
+                    s = scale * (kk @ q[i, h, :])
+                    e = np.exp(s - s.max())
+                    p = e / e.sum()
+                    o_i = p @ vv
+                    dp = vv @ do[i, h, :]
+                    D = do[i, h, :] @ o_i
+                    at = int(np.searchsorted(ks, j))
+                    acc_v += p[at] * do[i, h, :]
+                    acc_k += scale * p[at] * (dp[at] - D) * q[i, h, :]
             dk[(j, kv)] = acc_k
             dv[(j, kv)] = acc_v
     return dk, dv

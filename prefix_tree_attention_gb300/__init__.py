@@ -49,6 +49,11 @@ _sig = {
     "tree_packing_trie_arrays": (ctypes.c_int, [_P, _I32, _P, _P, _P, _P, _P]),
     "tree_packing_seq_indices": (ctypes.c_int, [_P, _I32, _I32, _P, _I32]),
     "tree_debug_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
+    "tree_attn_bwd_prepare": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _P, _SZ, _P, _P]),
+    "tree_attn_bwd_main": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32,
+                                          _P, _P, _P, _SZ, _P, _P]),
+    "tree_attn_bwd_finish": (ctypes.c_int, [_I32, _I32, _I32, _F32, _P, _SZ, _P, _P, _P]),
+    "tree_launch_count": (ctypes.c_uint64, []),
 }
 for _name, (_res, _args) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -169,6 +174,40 @@ def tree_attn_bwd(q, k, v, o, d_o, lse, key_reach, blockmap, dq, dk, dv, workspa
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o), _ptr(lse), _ptr(key_reach),
         _ptr(blockmap), T, Hq, Hkv, d, scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream_ptr(stream)))
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def tree_attn_bwd_prepare(o, d_o, lse, workspace, dev_status, stream=None):
+    T, Hq, d = o.shape
+    _check("tree_attn_bwd_prepare", _lib.tree_attn_bwd_prepare(
+        _ptr(o), _ptr(d_o), _ptr(lse), T, Hq, d, _ptr(workspace), _nbytes(workspace),
+        _ptr(dev_status), _stream_ptr(stream)))
+
+
+def tree_attn_bwd_main(q, k, v, d_o, key_reach, blockmap, dk, dv, workspace, dev_status,
+                       scale=None, stream=None):
+    T, Hq, d = q.shape
+    scale = d ** -0.5 if scale is None else float(scale)
+    _check("tree_attn_bwd_main", _lib.tree_attn_bwd_main(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(d_o), _ptr(key_reach), _ptr(blockmap), T, Hq,
+        k.shape[1], d, scale, _ptr(dk), _ptr(dv), _ptr(workspace), _nbytes(workspace),
+        _ptr(dev_status), _stream_ptr(stream)))
+
+
+def tree_attn_bwd_finish(workspace, dq, dev_status, scale=None, stream=None):
+    T, Hq, d = dq.shape
+    scale = d ** -0.5 if scale is None else float(scale)
+    _check("tree_attn_bwd_finish", _lib.tree_attn_bwd_finish(
+        T, Hq, d, scale, _ptr(workspace), _nbytes(workspace), _ptr(dq), _ptr(dev_status),
+        _stream_ptr(stream)))
+
+
+def launch_count() -> int:
+    """Kernels the library has queued so far in this process."""
+    return int(_lib.tree_launch_count())
 
 
 def tree_debug_wait_timeout(dev_status, limit_ns: int, stream=None):

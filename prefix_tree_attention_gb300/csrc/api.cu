@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -16,12 +17,23 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
                             int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o, float* lse,
                             int32_t* status, cudaStream_t s);
 size_t attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d);
-cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const void* o, const void* d_o,
-                            const float* lse, const int32_t* key_reach, const void* blockmap,
-                            int32_t T_pad, int32_t Hq, int32_t Hkv, int32_t d, float scale,
-                            void* dq, void* dk, void* dv, void* workspace, int32_t* status,
-                            cudaStream_t s, int num_sms);
+cudaError_t launch_attn_bwd_prepare(const void* o, const void* d_o, const float* lse,
+                                    int32_t T_pad, int32_t Hq, int32_t d, void* workspace,
+                                    int32_t* status, cudaStream_t s, int num_sms);
+cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo,
+                                 const int32_t* key_reach, const void* blockmap, int32_t T_pad,
+                                 int32_t Hq, int32_t Hkv, int32_t d, float scale, void* dk,
+                                 void* dv, void* workspace, int32_t* status, cudaStream_t s);
+cudaError_t launch_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
+                                   void* workspace, void* dq, int32_t* status, cudaStream_t s,
+                                   int num_sms);
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+uint64_t launches_total() { return g_launches.load(); }
 }  // namespace tree
 
 namespace {
@@ -168,6 +180,61 @@ size_t tree_attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d) {
   return tree::attn_bwd_workspace_bytes(T_pad, Hq, d);
 }
 
+tree_status_t tree_attn_bwd_prepare(const void* o, const void* d_o, const float* lse,
+                                    int32_t T_pad, int32_t Hq, int32_t d, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status,
+                                    tree_stream_t stream) {
+  tree_status_t st = check_attn_shape(T_pad, Hq, 1, d);
+  if (st != TREE_OK) return st;
+  if (!dev_status) return TREE_ERR_INVALID_ARG;
+  if (T_pad == 0) return TREE_OK;
+  if (!o || !d_o || !lse || !workspace) return TREE_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(d_o) || !aligned16(lse) || !aligned16(workspace))
+    return TREE_ERR_ALIGNMENT;
+  if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
+  return cuda_result(tree::launch_attn_bwd_prepare(o, d_o, lse, T_pad, Hq, d, workspace,
+                                                   dev_status, stream, num_sms_current()));
+}
+
+tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v, const void* d_o,
+                                 const int32_t* key_reach, const void* blockmap, int32_t T_pad,
+                                 int32_t Hq, int32_t Hkv, int32_t d, float scale, void* dk,
+                                 void* dv, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_status, tree_stream_t stream) {
+  tree_status_t st = check_attn_shape(T_pad, Hq, Hkv, d);
+  if (st != TREE_OK) return st;
+  if (!dev_status) return TREE_ERR_INVALID_ARG;
+  if (T_pad == 0) return TREE_OK;
+  if (!q || !k || !v || !d_o || !key_reach || !blockmap || !dk || !dv || !workspace)
+    return TREE_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, d_o, key_reach, blockmap, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return TREE_ERR_ALIGNMENT;
+  if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
+      !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&tdo, d_o, T_pad, Hq, d))
+    return TREE_ERR_CUDA;
+  return cuda_result(tree::launch_attn_bwd_main(tq, tk, tv, tdo, key_reach, blockmap, T_pad, Hq,
+                                                Hkv, d, scale, dk, dv, workspace, dev_status,
+                                                stream));
+}
+
+tree_status_t tree_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
+                                   const void* workspace, size_t workspace_bytes, void* dq,
+                                   int32_t* dev_status, tree_stream_t stream) {
+  tree_status_t st = check_attn_shape(T_pad, Hq, 1, d);
+  if (st != TREE_OK) return st;
+  if (!dev_status) return TREE_ERR_INVALID_ARG;
+  if (T_pad == 0) return TREE_OK;
+  if (!workspace || !dq) return TREE_ERR_INVALID_ARG;
+  if (!aligned16(workspace) || !aligned16(dq)) return TREE_ERR_ALIGNMENT;
+  if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
+  return cuda_result(tree::launch_attn_bwd_finish(T_pad, Hq, d, scale,
+                                                  const_cast<void*>(workspace), dq, dev_status,
+                                                  stream, num_sms_current()));
+}
+
 tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                             const void* d_o, const float* lse, const int32_t* key_reach,
                             const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
@@ -181,17 +248,16 @@ tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v, const v
   if (!q || !k || !v || !o || !d_o || !lse || !key_reach || !blockmap || !dq || !dk || !dv ||
       !workspace)
     return TREE_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, o, d_o, lse, key_reach, blockmap, dq, dk, dv, workspace};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return TREE_ERR_ALIGNMENT;
-  if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
-  CUtensorMap tq, tk, tv, tdo;
-  if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
-      !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&tdo, d_o, T_pad, Hq, d))
-    return TREE_ERR_CUDA;
-  return cuda_result(tree::launch_attn_bwd(tq, tk, tv, tdo, o, d_o, lse, key_reach, blockmap,
-                                           T_pad, Hq, Hkv, d, scale, dq, dk, dv, workspace,
-                                           dev_status, stream, num_sms_current()));
+  st = tree_attn_bwd_prepare(o, d_o, lse, T_pad, Hq, d, workspace, workspace_bytes, dev_status,
+                             stream);
+  if (st != TREE_OK) return st;
+  st = tree_attn_bwd_main(q, k, v, d_o, key_reach, blockmap, T_pad, Hq, Hkv, d, scale, dk, dv,
+                          workspace, workspace_bytes, dev_status, stream);
+  if (st != TREE_OK) return st;
+  return tree_attn_bwd_finish(T_pad, Hq, d, scale, workspace, workspace_bytes, dq, dev_status,
+                              stream);
 }
+
+uint64_t tree_launch_count(void) { return tree::launches_total(); }
 
 }  // extern "C"

@@ -395,32 +395,24 @@ tree_attn_bwd_dq_kernel(const float* dq_acc, __nv_bfloat16* dq, int64_t n8, floa
   }
 }
 
-template <int D>
-cudaError_t launch_bwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const void* o, const void* d_o,
-                         const float* lse, BwdParams p, void* dq, float* lse2_ws, float* dd_ws,
-                         cudaStream_t s, int num_sms) {
-  const int64_t rows = static_cast<int64_t>(p.T_pad) * p.Hq;
-  int prep_blocks = static_cast<int>((rows * 32 + 255) / 256);
-  if (prep_blocks > num_sms * 16) prep_blocks = num_sms * 16;
-  tree_attn_bwd_prep_kernel<D><<<prep_blocks, 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(d_o), lse, dd_ws,
-      lse2_ws, p.dq_acc, p.T_pad, p.Hq, p.status);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const size_t smem = sizeof(BwdSmem<D>);
-  e = cudaFuncSetAttribute(tree_attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  tree_attn_bwd_kernel<D><<<p.nb * p.Hkv, kBwdThreads, smem, s>>>(tq, tk, tv, tdo, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int64_t n8 = rows * D / 8;
-  int cv_blocks = static_cast<int>((n8 + 255) / 256);
-  if (cv_blocks > num_sms * 16) cv_blocks = num_sms * 16;
-  tree_attn_bwd_dq_kernel<<<cv_blocks, 256, 0, s>>>(p.dq_acc, static_cast<__nv_bfloat16*>(dq),
-                                                   n8, p.scale, p.status);
-  return cudaGetLastError();
+struct BwdWorkspace {
+  float* dq_acc;   // [T_pad, Hq, D]
+  float* dd;       // [Hq, T_pad]
+  float* lse2;     // [Hq, T_pad]
+};
+
+BwdWorkspace carve(void* workspace, int32_t T_pad, int32_t Hq, int32_t d) {
+  const size_t rows = static_cast<size_t>(T_pad) * Hq;
+  BwdWorkspace w;
+  w.dq_acc = static_cast<float*>(workspace);
+  w.dd = w.dq_acc + rows * d;
+  w.lse2 = w.dd + rows;
+  return w;
+}
+
+int grid_cap(int64_t blocks, int num_sms) {
+  const int64_t cap = static_cast<int64_t>(num_sms) * 16;
+  return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
 }
 
 }  // namespace
@@ -430,22 +422,36 @@ size_t attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d) {
   return rows * d * sizeof(float) + 2 * rows * sizeof(float);
 }
 
-cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const void* o, const void* d_o,
-                            const float* lse, const int32_t* key_reach, const void* blockmap,
-                            int32_t T_pad, int32_t Hq, int32_t Hkv, int32_t d, float scale,
-                            void* dq, void* dk, void* dv, void* workspace, int32_t* status,
-                            cudaStream_t s, int num_sms) {
-  const size_t rows = static_cast<size_t>(T_pad) * Hq;
-  float* dq_acc = static_cast<float*>(workspace);
-  float* dd_ws = dq_acc + rows * d;
-  float* lse2_ws = dd_ws + rows;
+cudaError_t launch_attn_bwd_prepare(const void* o, const void* d_o, const float* lse,
+                                    int32_t T_pad, int32_t Hq, int32_t d, void* workspace,
+                                    int32_t* status, cudaStream_t s, int num_sms) {
+  BwdWorkspace w = carve(workspace, T_pad, Hq, d);
+  const int64_t rows = static_cast<int64_t>(T_pad) * Hq;
+  const int blocks = grid_cap((rows * 32 + 255) / 256, num_sms);
+  const auto* po = static_cast<const __nv_bfloat16*>(o);
+  const auto* pd = static_cast<const __nv_bfloat16*>(d_o);
+  if (d == 64)
+    tree_attn_bwd_prep_kernel<64><<<blocks, 256, 0, s>>>(po, pd, lse, w.dd, w.lse2, w.dq_acc,
+                                                         T_pad, Hq, status);
+  else
+    tree_attn_bwd_prep_kernel<128><<<blocks, 256, 0, s>>>(po, pd, lse, w.dd, w.lse2, w.dq_acc,
+                                                          T_pad, Hq, status);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo,
+                                 const int32_t* key_reach, const void* blockmap, int32_t T_pad,
+                                 int32_t Hq, int32_t Hkv, int32_t d, float scale, void* dk,
+                                 void* dv, void* workspace, int32_t* status, cudaStream_t s) {
+  BwdWorkspace w = carve(workspace, T_pad, Hq, d);
   BwdParams p;
   p.key_reach = key_reach;
   p.blockmap = static_cast<const int32_t*>(blockmap);
-  p.lse2 = lse2_ws;
-  p.dd = dd_ws;
-  p.dq_acc = dq_acc;
+  p.lse2 = w.lse2;
+  p.dd = w.dd;
+  p.dq_acc = w.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.T_pad = T_pad;
@@ -455,8 +461,34 @@ cudaError_t launch_attn_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
-  return d == 64 ? launch_bwd_d<64>(tq, tk, tv, tdo, o, d_o, lse, p, dq, lse2_ws, dd_ws, s, num_sms)
-                 : launch_bwd_d<128>(tq, tk, tv, tdo, o, d_o, lse, p, dq, lse2_ws, dd_ws, s, num_sms);
+  const int grid = p.nb * Hkv;
+  cudaError_t e;
+  if (d == 64) {
+    e = cudaFuncSetAttribute(tree_attn_bwd_kernel<64>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(BwdSmem<64>)));
+    if (e != cudaSuccess) return e;
+    tree_attn_bwd_kernel<64><<<grid, kBwdThreads, sizeof(BwdSmem<64>), s>>>(tq, tk, tv, tdo, p);
+  } else {
+    e = cudaFuncSetAttribute(tree_attn_bwd_kernel<128>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(BwdSmem<128>)));
+    if (e != cudaSuccess) return e;
+    tree_attn_bwd_kernel<128><<<grid, kBwdThreads, sizeof(BwdSmem<128>), s>>>(tq, tk, tv, tdo, p);
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
+                                   void* workspace, void* dq, int32_t* status, cudaStream_t s,
+                                   int num_sms) {
+  BwdWorkspace w = carve(workspace, T_pad, Hq, d);
+  const int64_t n8 = static_cast<int64_t>(T_pad) * Hq * d / 8;
+  tree_attn_bwd_dq_kernel<<<grid_cap((n8 + 255) / 256, num_sms), 256, 0, s>>>(
+      w.dq_acc, static_cast<__nv_bfloat16*>(dq), n8, scale, status);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 }  // namespace tree

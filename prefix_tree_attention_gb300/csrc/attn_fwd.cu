@@ -198,29 +198,24 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int k = 0; k < ntiles; ++k) {
         if (!(ok = mbar_wait_warp(&sm.s_full[t], k & 1, ab))) break;
         tc_fence_after();
-        float x[kBlock];
+        // Two passes over the S row in TMEM keep the register footprint low:
+        // pass 1 finds the row max, pass 2 reloads, exponentiates and packs.
+        const bool partial = k >= nfull;
+        const int32_t* rch = sm.reach[k & 1];
+        const int32_t j0 = tiles[k] * kBlock;
+        float mt = -INFINITY;
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t reg[32];
           tmem_ld32(s_addr + c4 * 32, reg);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[c4 * 32 + e] = __uint_as_float(reg[e]);
-        }
-        if (k >= nfull) {
-          const int32_t* rch = sm.reach[k & 1];
-          const int32_t j0 = tiles[k] * kBlock;
-#pragma unroll
-          for (int c = 0; c < kBlock; ++c) {
-            const bool vis = (j0 + c <= i) && (i <= rch[c]);
-            x[c] = vis ? x[c] * p.scale_log2 : -INFINITY;
+          for (int e = 0; e < 32; ++e) {
+            const int c = c4 * 32 + e;
+            float xv = __uint_as_float(reg[e]) * p.scale_log2;
+            if (partial && !((j0 + c <= i) && (i <= rch[c]))) xv = -INFINITY;
+            mt = fmaxf(mt, xv);
           }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kBlock; ++c) x[c] *= p.scale_log2;
         }
-        float mt = x[0];
-#pragma unroll
-        for (int c = 1; c < kBlock; ++c) mt = fmaxf(mt, x[c]);
         const float mnew = fmaxf(m, mt);
         if (mnew > m + kRescaleThreshold) {
           const float alpha = ex2(m - mnew);   // 0 when m = -inf
@@ -239,13 +234,26 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
           m = mnew;
         }
         const float msub = (m == -INFINITY) ? 0.f : m;
+        // Columns c2*64 .. c2*64+63 are read before their packed P words are
+        // written to columns c2*32 .. c2*32+31, so no unread score is lost.
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t pk[32];
+          uint32_t ra[32], rb[32], pk[32];
+          tmem_ld32(s_addr + c2 * 64, ra);
+          tmem_ld32(s_addr + c2 * 64 + 32, rb);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2(x[c2 * 64 + 2 * e] - msub);
-            const float p1 = ex2(x[c2 * 64 + 2 * e + 1] - msub);
+            const int c = c2 * 64 + 2 * e;
+            const uint32_t* src = e < 16 ? ra : rb;
+            const int off = (e < 16 ? 2 * e : 2 * e - 32);
+            float x0 = __uint_as_float(src[off]) * p.scale_log2;
+            float x1 = __uint_as_float(src[off + 1]) * p.scale_log2;
+            if (partial) {
+              if (!((j0 + c <= i) && (i <= rch[c]))) x0 = -INFINITY;
+              if (!((j0 + c + 1 <= i) && (i <= rch[c + 1]))) x1 = -INFINITY;
+            }
+            const float p0 = ex2(x0 - msub);
+            const float p1 = ex2(x1 - msub);
             l += p0 + p1;
             pk[e] = pack_bf16x2(p0, p1);
           }
@@ -302,6 +310,7 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   tree_attn_fwd_kernel<D><<<grid, kFwdThreads, smem, s>>>(tq, tk, tv, p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

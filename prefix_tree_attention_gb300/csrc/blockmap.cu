@@ -182,6 +182,7 @@ cudaError_t launch_blockmap_build(const int32_t* key_reach, int32_t T_pad, void*
   k_ptrs<<<1, 1024, 0, s>>>(bm, status);
   k_fill<<<warp_grid, 32 * kWarpsPerCta, 0, s>>>(bm, status);
   k_order<<<(2 * bm.nb + 255) / 256, 256, 0, s>>>(bm, status);
+  count_launches(5);
   return cudaGetLastError();
 }
 

@@ -36,6 +36,11 @@ __device__ __forceinline__ int ld_status(const int32_t* s) {
 }
 __device__ __forceinline__ void set_status(int32_t* s, int code) { atomicCAS(s, 0, code); }
 
+// Number of kernels this library has launched in the process (all entry
+// points); every launcher adds the launches it queues.
+void count_launches(int n);
+uint64_t launches_total();
+
 // Launchers (one translation unit each); all return cudaGetLastError().
 cudaError_t launch_pack_positions(const int32_t* token_node, int32_t T_pad,
                                   const int32_t* node_entry, const int32_t* node_exit,

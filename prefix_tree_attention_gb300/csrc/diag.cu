@@ -29,5 +29,6 @@ extern "C" tree_status_t tree_debug_wait_timeout(int32_t* dev_status, int64_t li
                                                  tree_stream_t stream) {
   if (!dev_status || limit_ns < 1000000 || limit_ns > 2000000000) return TREE_ERR_INVALID_ARG;
   tree::k_wait_probe<<<1, 32, 0, stream>>>(dev_status, static_cast<uint64_t>(limit_ns));
+  tree::count_launches(1);
   return cudaGetLastError() == cudaSuccess ? TREE_OK : TREE_ERR_CUDA;
 }

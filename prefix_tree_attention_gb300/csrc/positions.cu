@@ -263,6 +263,7 @@ cudaError_t launch_pack_positions(const int32_t* token_node, int32_t T_pad,
   k_scan_top<<<1, kScanThreads, 0, s>>>(w, n_tiles, status);
   k_finalize<<<n_tiles, kScanThreads, 0, s>>>(w, token_node, T_pad, position_ids, key_reach,
                                               status);
+  count_launches(N > 0 ? 7 : 5);
   return cudaGetLastError();
 }
 

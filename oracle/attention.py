@@ -84,14 +84,15 @@ def backward(q, k, v, o, do, mask, scale=None):
     return dq, dk, dv
 
 
-def rows_forward_backward(q, k, v, do, packed, rows, heads, scale=None):
+def rows_forward_backward(q, k, v, do, packed, rows, heads, scale=None, key_grads=True):
     """Per-row forward and dQ for the listed query rows and query heads.
 
     Row ``i`` reads exactly the keys of its mask row (ancestor walk), so O,
     LSE and dQ of a row need nothing outside it.  Returns dicts keyed by
-    (row, head): ``o``, ``lse``, ``dq``; also the partial dK/dV those rows
-    contribute (``dk_part``/``dv_part``, dict keyed by kv head of
-    ``[T, d]`` arrays) — complete only when ``rows`` covers every row.
+    (row, head): ``o``, ``lse``, ``dq``; also (when ``key_grads``) the
+    partial dK/dV those rows contribute (``dk_part``/``dv_part``, dict keyed
+    by kv head of ``[T, d]`` arrays) — complete only when ``rows`` covers
+    every row.
     """
     d = q.shape[2]
     g = q.shape[1] // k.shape[1]
@@ -100,6 +101,7 @@ def rows_forward_backward(q, k, v, do, packed, rows, heads, scale=None):
     dk_part, dv_part = {}, {}
     for i in rows:
         keys = np.nonzero(mask_rows(packed, i, i + 1)[0])[0]
+        gathered = {}                     # kv head -> (K rows, V rows) of this row
         for h in heads:
             kv = h // g
             if keys.size == 0:
@@ -107,8 +109,9 @@ def rows_forward_backward(q, k, v, do, packed, rows, heads, scale=None):
                 out_lse[(i, h)] = -np.inf
                 out_dq[(i, h)] = np.zeros(d)
                 continue
-            kk = k[keys, kv, :]
-            vv = v[keys, kv, :]
+            if kv not in gathered:
+                gathered[kv] = (k[keys, kv, :], v[keys, kv, :])
+            kk, vv = gathered[kv]
             s = scale * (kk @ q[i, h, :])
             m = s.max()
             e = np.exp(s - m)
@@ -121,6 +124,8 @@ def rows_forward_backward(q, k, v, do, packed, rows, heads, scale=None):
             out_o[(i, h)] = o_i
             out_lse[(i, h)] = m + np.log(l)
             out_dq[(i, h)] = scale * (ds @ kk)
+            if not key_grads:
+                continue
             if kv not in dk_part:
                 dk_part[kv] = np.zeros((q.shape[0], d))
                 dv_part[kv] = np.zeros((q.shape[0], d))
@@ -157,19 +162,19 @@ def key_grads(q, k, v, do, packed, keys, kv_heads, scale=None):
         for kv in kv_heads:
             acc_k = np.zeros(d)
             acc_v = np.zeros(d)
-            for h in range(kv * g, (kv + 1) * g):
-                for i in rows:
+            for i in rows:
+                ks = row_keys[int(i)]
+                kk = k[ks, kv, :]
+                vv = v[ks, kv, :]
+                at = int(np.searchsorted(ks, j))
+                for h in range(kv * g, (kv + 1) * g):
                     # row i's softmax over its own keys, then key j's share
-                    ks = row_keys[int(i)]
-                    kk = k[ks, kv, :]
-                    vv = v[ks, kv, :]
                     s = scale * (kk @ q[i, h, :])
                     e = np.exp(s - s.max())
                     p = e / e.sum()
                     o_i = p @ vv
                     dp = vv @ do[i, h, :]
                     D = do[i, h, :] @ o_i
-                    at = int(np.searchsorted(ks, j))
                     acc_v += p[at] * do[i, h, :]
                     acc_k += scale * p[at] * (dp[at] - D) * q[i, h, :]
             dk[(j, kv)] = acc_k

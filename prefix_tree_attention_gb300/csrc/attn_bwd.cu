@@ -194,6 +194,13 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         umma_commit(&sm.dp_full);
         if (!(ok = mbar_wait(&sm.ew_done, n & 1, ab))) break;
         tc_fence_after();
+        // dQ first: its read-out and atomics then overlap the dV/dK MMAs,
+        // and the next dP^T (same TMEM columns) is not held up by them.
+#pragma unroll
+        for (int kk = 0; kk < kBlock / 16; ++kk)
+          umma_ss(tbase + kDQ, sdesc_sw128(dsbase + kk * 2048, kBlock * 128, 1024),
+                  sdesc_sw128(kbase + kk * 2048, kBlock * 128, 1024), kIdescDQ, kk > 0);
+        umma_commit(&sm.dq_full);
         // P^T for queries 0-63 sits at [256,288), 64-127 at [320,352);
         // dS^T at [288,320) and [352,384).
 #pragma unroll
@@ -209,11 +216,6 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                   kIdescTS, (n > 0 || kk > 0));
         }
         umma_commit(&sm.dvdk_done);
-#pragma unroll
-        for (int kk = 0; kk < kBlock / 16; ++kk)
-          umma_ss(tbase + kDQ, sdesc_sw128(dsbase + kk * 2048, kBlock * 128, 1024),
-                  sdesc_sw128(kbase + kk * 2048, kBlock * 128, 1024), kIdescDQ, kk > 0);
-        umma_commit(&sm.dq_full);
         umma_commit(&sm.empty[s]);
       }
       if (!ok) {

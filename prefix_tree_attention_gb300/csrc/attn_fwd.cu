@@ -217,21 +217,27 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         }
         const float mnew = fmaxf(m, mt);
-        if (mnew > m + kRescaleThreshold) {
-          const float alpha = ex2(m - mnew);   // 0 when m = -inf
-          if (k > 0) {
-#pragma unroll
-            for (int c4 = 0; c4 < D / 32; ++c4) {
-              uint32_t reg[32];
-              tmem_ld32(o_addr + c4 * 32, reg);
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                reg[e] = __float_as_uint(__uint_as_float(reg[e]) * alpha);
-              tmem_st32(o_addr + c4 * 32, reg);
-            }
-          }
+        // The decision is per row, but tcgen05.ld/st are warp-collective: the
+        // O rescale runs for the whole warp when any of its rows needs it,
+        // with alpha = 1 on the rows that do not.  (A row whose earlier tiles
+        // were all masked, e.g. one past a top-level subtree boundary inside
+        // the block, first sees a key at a later tile.)
+        const bool grow = mnew > m + kRescaleThreshold;
+        const float alpha = grow ? ex2(m - mnew) : 1.f;   // 0 when m = -inf
+        if (grow) {
           l *= alpha;
           m = mnew;
+        }
+        if (k > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t reg[32];
+            tmem_ld32(o_addr + c4 * 32, reg);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              reg[e] = __float_as_uint(__uint_as_float(reg[e]) * alpha);
+            tmem_st32(o_addr + c4 * 32, reg);
+          }
         }
         const float msub = (m == -INFINITY) ? 0.f : m;
         // Columns c2*64 .. c2*64+63 are read before their packed P words are

@@ -248,6 +248,25 @@ def test_random_tries_dense(Hq, Hkv, d, seed):
         check_integer_outputs(p, bufs)
 
 
+@pytest.mark.parametrize("Hq,Hkv,d", [(4, 1, 128), (2, 2, 64)])
+def test_top_level_boundaries_inside_blocks(Hq, Hkv, d):
+    # Several top-level subtrees whose boundaries fall inside 128-token
+    # blocks: rows just past a boundary see nothing in the first listed
+    # tiles of their block and meet their first visible key later on.
+    rng = W.SplitMix64(77)
+    seqs = []
+    for s in range(6):
+        L = rng.randint(150, 700)
+        seqs.append([1000 * (s + 1) + t for t in range(L)])
+    seqs.append(seqs[1][:200] + [99000 + t for t in range(rng.randint(50, 300))])
+    _, refs = pack_both(seqs, 8192)
+    for p in refs:
+        starts = [p.node_start[n] for n in range(p.n_nodes) if p.node_parent[n] < 0]
+        assert any(s_ % 128 for s_ in starts[1:])
+        bufs = check_attention_dense(p, Hq, Hkv, d, seed=9)
+        check_integer_outputs(p, bufs)
+
+
 def test_full_tiles_long_prefix():
     rng = W.SplitMix64(21)
     prefix = [rng.randint(1, 50) for _ in range(900)]
@@ -331,7 +350,8 @@ def check_full_size(key, trie_indices, n_rows=6, n_keys=3):
         q, k, v, do = (_f64(t[n]) for n in ("q", "k", "v", "do"))
         rows = _sampled_rows(p, n_rows, rng)
         heads = range(wl.Hq)
-        ro, rl, rdq, _, _ = OA.rows_forward_backward(q, k, v, do, p, rows, heads)
+        ro, rl, rdq, _, _ = OA.rows_forward_backward(q, k, v, do, p, rows, heads,
+                                                      key_grads=False)
         o_np, dq_np, lse_np = _f64(o), _f64(dq), lse.cpu().numpy()
         errs_o, errs_dq = [], []
         for i in rows:
@@ -370,7 +390,7 @@ def test_full_fanout():
 
 
 def test_full_grpo_sampled_tries():
-    check_full_size("grpo", [0, 25])
+    check_full_size("grpo", [25])
 
 
 def test_full_agent_sampled_tries():

@@ -114,6 +114,32 @@ TREE_API tree_status_t tree_pack_positions(const int32_t* token_node, int32_t T_
                                   tree_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * tree_pack_positions_noalloc — tree_pack_positions without a workspace.
+ *
+ * The pages have no counterpart; this entry point exists for callers that
+ * cannot allocate device memory at all — typically a plugin or custom
+ * operator inside a host framework that owns every device allocation and
+ * gives the operator only its input and output buffers, so it has no
+ * workspace to pass.  The library keeps the scratch in one file-scope device
+ * array of 1.75 MiB (held by every GPU that loads the library until the
+ * process exits), enough for T_pad <= 65536 and n_nodes <= 65536; larger
+ * sizes return TREE_ERR_WORKSPACE and launch nothing.  Nothing is allocated
+ * or freed, by the library or by anything it calls.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call re-initialises the scratch it uses before reading it.
+ * All calls share the one array, so calls whose work overlaps on the GPU
+ * (other streams, other host threads) race and must be serialised.
+ * Arguments, outputs and device-side errors are those of tree_pack_positions.
+ * ---------------------------------------------------------------------- */
+TREE_API tree_status_t tree_pack_positions_noalloc(const int32_t* token_node, int32_t T_pad,
+                                                   const int32_t* node_entry,
+                                                   const int32_t* node_exit, int32_t n_nodes,
+                                                   int32_t* position_ids, int32_t* key_reach,
+                                                   int32_t* dev_status, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * tree_blockmap_build — classify every 128x128 (query block, key block)
  * tile as EMPTY, FULL or PARTIAL and list the non-empty tiles.
  *

@@ -54,6 +54,7 @@ _sig = {
                                           _P, _P, _P, _SZ, _P, _P]),
     "tree_attn_bwd_finish": (ctypes.c_int, [_I32, _I32, _I32, _F32, _P, _SZ, _P, _P, _P]),
     "tree_launch_count": (ctypes.c_uint64, []),
+    "tree_pack_positions_noalloc": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P, _P, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -134,6 +135,21 @@ def tree_pack_positions(token_node, node_entry, node_exit, position_ids, key_rea
         _ptr(token_node), T_pad, _ptr(node_entry) if N else 0, _ptr(node_exit) if N else 0, N,
         _ptr(position_ids), _ptr(key_reach), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream_ptr(stream)))
+
+
+def tree_pack_positions_noalloc(token_node, node_entry, node_exit, position_ids, key_reach,
+                                dev_status, stream=None):
+    """tree_pack_positions with the library's fixed device scratch array
+    (no workspace argument; T_pad and n_nodes up to 65536)."""
+    import torch
+    _need(token_node, torch.int32, "token_node")
+    for t, n in ((position_ids, "position_ids"), (key_reach, "key_reach")):
+        _need(t, torch.int32, n)
+    N = node_entry.numel()
+    _check("tree_pack_positions_noalloc", _lib.tree_pack_positions_noalloc(
+        _ptr(token_node), token_node.numel(), _ptr(node_entry) if N else 0,
+        _ptr(node_exit) if N else 0, N, _ptr(position_ids), _ptr(key_reach), _ptr(dev_status),
+        _stream_ptr(stream)))
 
 
 def tree_blockmap_build(key_reach, blockmap, dev_status, stream=None, block: int = BLOCK):

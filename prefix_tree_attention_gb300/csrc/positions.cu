@@ -25,6 +25,7 @@
 //  7 finalize     inclusive scan -> position ids and key_reach; a pad whose
 //                 count is non-zero lies inside a subtree span -> malformed
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -268,3 +269,81 @@ cudaError_t launch_pack_positions(const int32_t* token_node, int32_t T_pad,
 }
 
 }  // namespace tree
+
+// ---------------------------------------------------------------------------
+// tree_pack_positions_noalloc: the same kernels with their scratch in a
+// file-scope device array instead of a caller-provided workspace.
+//
+// Some callers cannot allocate device memory: a plugin or custom operator
+// running inside a host framework that owns all device memory hands its
+// kernels only their input and output buffers, so there is nowhere to get a
+// workspace from.  For them this entry point keeps the scratch of
+// tree_pack_positions in `g_positions_scratch`, a fixed 1.75 MiB array that
+// every GPU loading the library holds until the process exits.  The host
+// cannot pass the array's name to a kernel (in host code it names a host-side
+// stand-in, not device memory), so the first call on each device looks up the
+// device address with cudaGetSymbolAddress, with that device current, and
+// caches it; make that first call before any stream capture.
+namespace tree {
+namespace {
+
+constexpr int32_t kNoAllocMaxTokens = 65536;
+constexpr int32_t kNoAllocMaxNodes = 65536;
+constexpr size_t kNoAllocScratchBytes =
+    6 * ((sizeof(int32_t) * kNoAllocMaxNodes + 255) / 256 * 256) +
+    (sizeof(int32_t) * (kNoAllocMaxTokens + 1) + 255) / 256 * 256 +
+    (sizeof(int32_t) * ((kNoAllocMaxTokens + kScanTile - 1) / kScanTile + 1) + 255) / 256 * 256;
+
+__device__ __align__(256) uint8_t g_positions_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_positions_scratch on the current device (looked up
+// once per device).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_positions_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace tree
+
+extern "C" tree_status_t tree_pack_positions_noalloc(const int32_t* token_node, int32_t T_pad,
+                                                     const int32_t* node_entry,
+                                                     const int32_t* node_exit, int32_t n_nodes,
+                                                     int32_t* position_ids, int32_t* key_reach,
+                                                     int32_t* dev_status, tree_stream_t stream) {
+  if (T_pad < 0 || n_nodes < 0 || !dev_status) return TREE_ERR_INVALID_ARG;
+  if (T_pad % tree::kBlock) return TREE_ERR_ALIGNMENT;
+  if (T_pad > tree::kNoAllocMaxTokens || n_nodes > tree::kNoAllocMaxNodes)
+    return TREE_ERR_WORKSPACE;   // beyond the fixed scratch array
+  if (T_pad == 0) return TREE_OK;
+  if (!token_node || !position_ids || !key_reach || (n_nodes > 0 && (!node_entry || !node_exit)))
+    return TREE_ERR_INVALID_ARG;
+  if (n_nodes > T_pad) return TREE_ERR_INVALID_ARG;
+  if (tree::pack_positions_workspace_bytes(T_pad, n_nodes) > tree::kNoAllocScratchBytes)
+    return TREE_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (tree::scratch_address(&scratch) != cudaSuccess) return TREE_ERR_CUDA;
+  // Every call re-initialises the scratch it uses (the first kernel), so the
+  // previous call's contents never leak into this one.  Calls that overlap on
+  // the GPU (different streams, or different host threads on one device)
+  // share this one array and race: serialise them.
+  cudaError_t e = tree::launch_pack_positions(token_node, T_pad, node_entry, node_exit, n_nodes,
+                                              position_ids, key_reach, scratch, dev_status,
+                                              stream);
+  return e == cudaSuccess ? TREE_OK : TREE_ERR_CUDA;
+}

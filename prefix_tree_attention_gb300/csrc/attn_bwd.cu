@@ -88,8 +88,13 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BlockmapView bm{p.nb, const_cast<int32_t*>(p.blockmap)};
-  const int32_t kb = bm.col_order()[blockIdx.x / p.Hkv];
-  const int32_t kvh = blockIdx.x % p.Hkv;
+  // CTAs run kv-head-major with key blocks ascending: the CTAs resident at
+  // any moment hold neighbouring key blocks of one kv head, so they stream
+  // the same Q/dO tiles and add into the same dQ rows close together in
+  // time (L2 reuse).  Early key blocks carry the longest columns, so the
+  // order is also roughly heaviest first within each head.
+  const int32_t kvh = blockIdx.x / p.nb;
+  const int32_t kb = blockIdx.x % p.nb;
   const int32_t g = p.Hq / p.Hkv;
   const int32_t col_hi = bm.col_hi()[kb];
   const int32_t col_full_hi = bm.col_full_hi()[kb];
@@ -139,8 +144,8 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int n = 0; n < nsteps; ++n) {
         const int s = n & 1;
         if (n >= 2 && !mbar_wait(&sm.empty[s], ((n >> 1) - 1) & 1, ab)) break;
-        const int32_t h = kvh * g + n / col_len;
-        const int32_t qa = kb + n % col_len;
+        const int32_t h = kvh * g + n % g;      // query block outer, heads inner
+        const int32_t qa = kb + n / g;
         mbar_arrive_expect_tx(&sm.full[s], 2 * kTileBytes + 2 * kBlock * 4);
         for (int hf = 0; hf < kHalves; ++hf) {
           tma_load_3d(sm.q[s] + hf * kBlock * 64, &tm_q, &sm.full[s], hf * 64, h, qa * kBlock);
@@ -234,45 +239,60 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool ok = true;
     for (int n = 0; ok && n < nsteps; ++n) {
       const int s = n & 1;
-      const int32_t h = kvh * g + n / col_len;
-      const int32_t qa = kb + n % col_len;
+      const int32_t h = kvh * g + n % g;
+      const int32_t qa = kb + n / g;
       const bool partial = (qa == kb) || (qa > col_full_hi);
       if (!(ok = mbar_wait_warp(&sm.s_full, n & 1, ab))) break;
       tc_fence_after();
       float pv[64];
       {
-        uint32_t reg[32];
+        uint32_t ra[32], rb[32];
+        tmem_ld32x2(tbase + lane_off + kS + w * 64, tbase + lane_off + kS + w * 64 + 32, ra, rb);
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          tmem_ld32(tbase + lane_off + kS + w * 64 + c2 * 32, reg);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pv[c2 * 32 + e] = __uint_as_float(reg[e]);
+        for (int e = 0; e < 32; ++e) {
+          pv[e] = __uint_as_float(ra[e]);
+          pv[32 + e] = __uint_as_float(rb[e]);
         }
       }
-      const float* lse2 = sm.lse2[s] + w * 64;
-      const int32_t q0 = qa * kBlock + w * 64;
+      // P^T = 2^(S^T*scale*log2e - lse2); lse2 read 4 at a time (broadcast).
+      const float4* lse4 = reinterpret_cast<const float4*>(sm.lse2[s] + w * 64);
+      const float sl2 = p.scale_log2;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const bool vis = !partial || (jkey <= q0 + c && q0 + c <= reach);
-        const float e = ex2(pv[c] * p.scale_log2 - lse2[c]);
-        pv[c] = vis ? e : 0.f;
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = lse4[c4];
+        pv[4 * c4 + 0] = ex2(fmaf(pv[4 * c4 + 0], sl2, -l4.x));
+        pv[4 * c4 + 1] = ex2(fmaf(pv[4 * c4 + 1], sl2, -l4.y));
+        pv[4 * c4 + 2] = ex2(fmaf(pv[4 * c4 + 2], sl2, -l4.z));
+        pv[4 * c4 + 3] = ex2(fmaf(pv[4 * c4 + 3], sl2, -l4.w));
+      }
+      if (partial) {   // warp-uniform: only PARTIAL tiles evaluate the mask
+        const int32_t q0 = qa * kBlock + w * 64;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (!(jkey <= q0 + c && q0 + c <= reach)) pv[c] = 0.f;
       }
       if (!(ok = mbar_wait_warp(&sm.dp_full, n & 1, ab))) break;
       tc_fence_after();
       uint32_t pk[32], dsw[32];
       {
-        const float* dd = sm.dd[s] + w * 64;
-        uint32_t reg[32];
+        const float4* dd4 = reinterpret_cast<const float4*>(sm.dd[s] + w * 64);
+        uint32_t ra[32], rb[32];
+        tmem_ld32x2(tbase + lane_off + kDP + w * 64, tbase + lane_off + kDP + w * 64 + 32, ra, rb);
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
-          tmem_ld32(tbase + lane_off + kDP + w * 64 + c2 * 32, reg);
+          const uint32_t* reg = c2 == 0 ? ra : rb;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = c2 * 32 + 2 * e;
-            const float ds0 = pv[c] * (__uint_as_float(reg[2 * e]) - dd[c]);
-            const float ds1 = pv[c + 1] * (__uint_as_float(reg[2 * e + 1]) - dd[c + 1]);
-            pk[c2 * 16 + e] = pack_bf16x2(pv[c], pv[c + 1]);
-            dsw[c2 * 16 + e] = pack_bf16x2(ds0, ds1);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 d4 = dd4[c2 * 8 + e4];
+            const int c = c2 * 32 + 4 * e4;
+            const float ds0 = pv[c + 0] * (__uint_as_float(reg[4 * e4 + 0]) - d4.x);
+            const float ds1 = pv[c + 1] * (__uint_as_float(reg[4 * e4 + 1]) - d4.y);
+            const float ds2 = pv[c + 2] * (__uint_as_float(reg[4 * e4 + 2]) - d4.z);
+            const float ds3 = pv[c + 3] * (__uint_as_float(reg[4 * e4 + 3]) - d4.w);
+            pk[c2 * 16 + 2 * e4] = pack_bf16x2(pv[c], pv[c + 1]);
+            pk[c2 * 16 + 2 * e4 + 1] = pack_bf16x2(pv[c + 2], pv[c + 3]);
+            dsw[c2 * 16 + 2 * e4] = pack_bf16x2(ds0, ds1);
+            dsw[c2 * 16 + 2 * e4 + 1] = pack_bf16x2(ds2, ds3);
           }
         }
       }
@@ -294,18 +314,31 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!(ok = mbar_wait_warp(&sm.dq_full, n & 1, ab))) break;
       tc_fence_after();
       float* dst = p.dq_acc + (static_cast<size_t>(qa * kBlock + r) * p.Hq + h) * D + w * (D / 2);
-#pragma unroll
-      for (int c2 = 0; c2 < D / 64; ++c2) {
-        uint32_t reg[32];
-        tmem_ld32(tbase + lane_off + kDQ + w * (D / 2) + c2 * 32, reg);
+      const uint32_t dq_col = tbase + lane_off + kDQ + w * (D / 2);
+      if constexpr (D == 128) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32x2(dq_col, dq_col + 32, ra, rb);
+        tc_fence_before();
+        mbar_arrive(&sm.dq_free);     // TMEM read done; the adds below need only registers
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          atomicAdd(reinterpret_cast<float4*>(dst + c2 * 32 + 4 * e),
-                    make_float4(__uint_as_float(reg[4 * e]), __uint_as_float(reg[4 * e + 1]),
-                                __uint_as_float(reg[4 * e + 2]), __uint_as_float(reg[4 * e + 3])));
+          red_add_v4(dst + 4 * e, __uint_as_float(ra[4 * e]), __uint_as_float(ra[4 * e + 1]),
+                     __uint_as_float(ra[4 * e + 2]), __uint_as_float(ra[4 * e + 3]));
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          red_add_v4(dst + 32 + 4 * e, __uint_as_float(rb[4 * e]),
+                     __uint_as_float(rb[4 * e + 1]), __uint_as_float(rb[4 * e + 2]),
+                     __uint_as_float(rb[4 * e + 3]));
+      } else {
+        uint32_t ra[32];
+        tmem_ld32(dq_col, ra);
+        tc_fence_before();
+        mbar_arrive(&sm.dq_free);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          red_add_v4(dst + 4 * e, __uint_as_float(ra[4 * e]), __uint_as_float(ra[4 * e + 1]),
+                     __uint_as_float(ra[4 * e + 2]), __uint_as_float(ra[4 * e + 3]));
       }
-      tc_fence_before();
-      mbar_arrive(&sm.dq_free);
     }
     // ---------------------------------------------------------- epilogue
     __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(jkey) * p.Hkv + kvh) * D + w * (D / 2);
@@ -315,8 +348,8 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
       for (int c2 = 0; c2 < D / 64; ++c2) {
         uint32_t rv[32], rk[32];
-        tmem_ld32(tbase + lane_off + kDV + w * (D / 2) + c2 * 32, rv);
-        tmem_ld32(tbase + lane_off + kDK + w * (D / 2) + c2 * 32, rk);
+        tmem_ld32x2(tbase + lane_off + kDV + w * (D / 2) + c2 * 32,
+                    tbase + lane_off + kDK + w * (D / 2) + c2 * 32, rv, rk);
 #pragma unroll
         for (int e8 = 0; e8 < 4; ++e8) {
           uint4 a, b;

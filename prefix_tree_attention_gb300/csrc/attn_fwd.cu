@@ -76,8 +76,11 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BlockmapView bm{p.nb, const_cast<int32_t*>(p.blockmap)};
-  const int32_t qa = bm.row_order()[blockIdx.x / p.n_hgroups];
-  const int32_t h0 = (blockIdx.x % p.n_hgroups) * p.heads_per_cta;
+  // Head-group-major order: the CTAs resident at any moment share one head
+  // group (so one kv head's K/V stays hot in L2) and take query blocks
+  // heaviest row first.
+  const int32_t qa = bm.row_order()[blockIdx.x % p.nb];
+  const int32_t h0 = (blockIdx.x / p.nb) * p.heads_per_cta;
   const int nh = p.heads_per_cta;
   const int32_t kvh = h0 / (p.Hq / p.Hkv);
   const int32_t ntiles = bm.row_cnt()[qa];
@@ -195,23 +198,70 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       const uint32_t o_addr = tbase + lane_off + 256 + t * 128;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
+      int32_t kb_next = ntiles > 0 ? tiles[0] : 0;
       for (int k = 0; k < ntiles; ++k) {
+        // the tile index is read before the wait so its latency overlaps it
+        const int32_t j0 = kb_next * kBlock;
+        if (k + 1 < ntiles) kb_next = tiles[k + 1];
         if (!(ok = mbar_wait_warp(&sm.s_full[t], k & 1, ab))) break;
         tc_fence_after();
-        // Two passes over the S row in TMEM keep the register footprint low:
-        // pass 1 finds the row max, pass 2 reloads, exponentiates and packs.
         const bool partial = k >= nfull;
         const int32_t* rch = sm.reach[k & 1];
-        const int32_t j0 = tiles[k] * kBlock;
+        const float sl2 = p.scale_log2;
+        // Common path: one pass against the running max of the earlier tiles
+        // (p = 2^(s*scale*log2e - m) in one FMA + ex2).  P stays in
+        // registers and is written over S only when no row's max grew by
+        // more than the threshold; otherwise S is still intact and the exact
+        // two-pass path below redoes the tile.  Rows with no running max yet
+        // (a row's first visible tile) always take the exact path.
+        bool exact = __any_sync(0xffffffffu, m == -INFINITY);
+        if (!exact) {
+          uint32_t pk0[32], pk1[32];
+          // four independent max/sum chains keep the FP pipes busy
+          float lt[4] = {0.f, 0.f, 0.f, 0.f};
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          const float nm = -m;
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t ra[32], rb[32];
+            tmem_ld32x2(s_addr + c2 * 64, s_addr + c2 * 64 + 32, ra, rb);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int c = c2 * 64 + 2 * e;
+              float s0 = __uint_as_float(e < 16 ? ra[2 * e] : rb[2 * e - 32]);
+              float s1 = __uint_as_float(e < 16 ? ra[2 * e + 1] : rb[2 * e - 31]);
+              if (partial) {
+                if (!((j0 + c <= i) && (i <= rch[c]))) s0 = -INFINITY;
+                if (!((j0 + c + 1 <= i) && (i <= rch[c + 1]))) s1 = -INFINITY;
+              }
+              mx[e & 3] = fmaxf(mx[e & 3], fmaxf(s0, s1));
+              const float p0 = ex2(fmaf(s0, sl2, nm));
+              const float p1 = ex2(fmaf(s1, sl2, nm));
+              lt[e & 3] += p0 + p1;
+              if (c2 == 0) pk0[e] = pack_bf16x2(p0, p1);
+              else pk1[e] = pack_bf16x2(p0, p1);
+            }
+          }
+          const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          exact = __any_sync(0xffffffffu, mraw * sl2 > m + kRescaleThreshold);
+          if (!exact) {
+            l += (lt[0] + lt[1]) + (lt[2] + lt[3]);
+            tmem_st32(s_addr, pk0);
+            tmem_st32(s_addr + 32, pk1);
+          }
+        }
+        if (exact) {
+        // Exact path: pass 1 finds the row max, pass 2 reloads, exponentiates
+        // and packs.
         float mt = -INFINITY;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t reg[32];
-          tmem_ld32(s_addr + c4 * 32, reg);
+        for (int c4 = 0; c4 < 4; c4 += 2) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32x2(s_addr + c4 * 32, s_addr + c4 * 32 + 32, ra, rb);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
+          for (int e = 0; e < 64; ++e) {
             const int c = c4 * 32 + e;
-            float xv = __uint_as_float(reg[e]) * p.scale_log2;
+            float xv = __uint_as_float(e < 32 ? ra[e] : rb[e - 32]) * p.scale_log2;
             if (partial && !((j0 + c <= i) && (i <= rch[c]))) xv = -INFINITY;
             mt = fmaxf(mt, xv);
           }
@@ -245,8 +295,7 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           uint32_t ra[32], rb[32], pk[32];
-          tmem_ld32(s_addr + c2 * 64, ra);
-          tmem_ld32(s_addr + c2 * 64 + 32, rb);
+          tmem_ld32x2(s_addr + c2 * 64, s_addr + c2 * 64 + 32, ra, rb);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int c = c2 * 64 + 2 * e;
@@ -265,6 +314,7 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
           tmem_st32(s_addr + c2 * 32, pk);
         }
+        }   // exact path
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full[t]);

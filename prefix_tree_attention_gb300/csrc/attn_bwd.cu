@@ -7,7 +7,8 @@
 // continuation, so its dK/dV sum over all of them.
 //
 // Kernels:
-//  a4 prep     D[h,i] = sum_d dO[i,h,d] O[i,h,d];  lse2 = LSE * log2(e);
+//  a4 prep     D[h,i] = sum_d dO[i,h,d] O[i,h,d];  lse2 = LSE * log2(e); both
+//              are stored negated (the main kernel adds them);
 //              the fp32 dQ accumulator is zeroed.
 //  a5 main     one CTA per (key block kb, kv head).  The key block's
 //              non-empty query tiles form the column run kb..col_hi of the
@@ -56,8 +57,8 @@ struct __align__(1024) BwdSmem {
 struct BwdParams {
   const int32_t* key_reach;
   const int32_t* blockmap;
-  const float* lse2;          // [Hq, T_pad]
-  const float* dd;            // [Hq, T_pad]
+  const float* lse2;          // [Hq, T_pad], -LSE * log2(e)
+  const float* dd;            // [Hq, T_pad], -D
   float* dq_acc;              // [T_pad, Hq, D]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -254,16 +255,20 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
           pv[32 + e] = __uint_as_float(rb[e]);
         }
       }
-      // P^T = 2^(S^T*scale*log2e - lse2); lse2 read 4 at a time (broadcast).
+      // P^T = 2^(S^T*scale*log2e - LSE*log2e) with paired FMAs; the negated
+      // LSE row is read 4 at a time (broadcast).
       const float4* lse4 = reinterpret_cast<const float4*>(sm.lse2[s] + w * 64);
       const float sl2 = p.scale_log2;
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l4 = lse4[c4];
-        pv[4 * c4 + 0] = ex2(fmaf(pv[4 * c4 + 0], sl2, -l4.x));
-        pv[4 * c4 + 1] = ex2(fmaf(pv[4 * c4 + 1], sl2, -l4.y));
-        pv[4 * c4 + 2] = ex2(fmaf(pv[4 * c4 + 2], sl2, -l4.z));
-        pv[4 * c4 + 3] = ex2(fmaf(pv[4 * c4 + 3], sl2, -l4.w));
+        float* x = pv + 4 * c4;
+        fma2(x[0], x[1], x[0], x[1], sl2, sl2, l4.x, l4.y);
+        fma2(x[2], x[3], x[2], x[3], sl2, sl2, l4.z, l4.w);
+        x[0] = ex2(x[0]);
+        x[1] = ex2(x[1]);
+        x[2] = ex2(x[2]);
+        x[3] = ex2(x[3]);
       }
       if (partial) {   // warp-uniform: only PARTIAL tiles evaluate the mask
         const int32_t q0 = qa * kBlock + w * 64;
@@ -283,12 +288,15 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
           const uint32_t* reg = c2 == 0 ? ra : rb;
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 d4 = dd4[c2 * 8 + e4];
+            const float4 d4 = dd4[c2 * 8 + e4];    // -D
             const int c = c2 * 32 + 4 * e4;
-            const float ds0 = pv[c + 0] * (__uint_as_float(reg[4 * e4 + 0]) - d4.x);
-            const float ds1 = pv[c + 1] * (__uint_as_float(reg[4 * e4 + 1]) - d4.y);
-            const float ds2 = pv[c + 2] * (__uint_as_float(reg[4 * e4 + 2]) - d4.z);
-            const float ds3 = pv[c + 3] * (__uint_as_float(reg[4 * e4 + 3]) - d4.w);
+            float t0, t1, t2, t3, ds0, ds1, ds2, ds3;
+            add2(t0, t1, __uint_as_float(reg[4 * e4 + 0]), __uint_as_float(reg[4 * e4 + 1]),
+                 d4.x, d4.y);
+            add2(t2, t3, __uint_as_float(reg[4 * e4 + 2]), __uint_as_float(reg[4 * e4 + 3]),
+                 d4.z, d4.w);
+            mul2(ds0, ds1, pv[c + 0], pv[c + 1], t0, t1);
+            mul2(ds2, ds3, pv[c + 2], pv[c + 3], t2, t3);
             pk[c2 * 16 + 2 * e4] = pack_bf16x2(pv[c], pv[c + 1]);
             pk[c2 * 16 + 2 * e4 + 1] = pack_bf16x2(pv[c + 2], pv[c + 3]);
             dsw[c2 * 16 + 2 * e4] = pack_bf16x2(ds0, ds1);
@@ -409,8 +417,9 @@ tree_attn_bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, con
     float4* z = reinterpret_cast<float4*>(dq_acc + row * D);
     for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lane == 0) {
-      dd[h * T_pad + i] = acc;
-      lse2[h * T_pad + i] = lse[h * T_pad + i] * 1.4426950408889634f;
+      // stored negated so the main kernel's paired FMA/add consume them directly
+      dd[h * T_pad + i] = -acc;
+      lse2[h * T_pad + i] = -lse[h * T_pad + i] * 1.4426950408889634f;
     }
   }
 }

@@ -33,6 +33,7 @@ namespace {
 
 constexpr int kFwdThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr float kGrowthLimit = 256.0f;     // 2^kRescaleThreshold
 
 template <int D>
 struct __align__(1024) FwdSmem {
@@ -217,9 +218,11 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         bool exact = __any_sync(0xffffffffu, m == -INFINITY);
         if (!exact) {
           uint32_t pk0[32], pk1[32];
-          // four independent max/sum chains keep the FP pipes busy
-          float lt[4] = {0.f, 0.f, 0.f, 0.f};
-          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          // Paired fp32 math, four independent sum chains, and the growth
+          // test on the packed bf16 P itself: P > 2^threshold exactly when
+          // the score exceeds the running max by more than the threshold.
+          float lt[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          uint32_t pmax[4] = {0u, 0u, 0u, 0u};
           const float nm = -m;
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2) {
@@ -228,24 +231,28 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const int c = c2 * 64 + 2 * e;
-              float s0 = __uint_as_float(e < 16 ? ra[2 * e] : rb[2 * e - 32]);
-              float s1 = __uint_as_float(e < 16 ? ra[2 * e + 1] : rb[2 * e - 31]);
+              float x0, x1;
+              fma2(x0, x1, __uint_as_float(e < 16 ? ra[2 * e] : rb[2 * e - 32]),
+                   __uint_as_float(e < 16 ? ra[2 * e + 1] : rb[2 * e - 31]), sl2, sl2, nm, nm);
               if (partial) {
-                if (!((j0 + c <= i) && (i <= rch[c]))) s0 = -INFINITY;
-                if (!((j0 + c + 1 <= i) && (i <= rch[c + 1]))) s1 = -INFINITY;
+                if (!((j0 + c <= i) && (i <= rch[c]))) x0 = -INFINITY;
+                if (!((j0 + c + 1 <= i) && (i <= rch[c + 1]))) x1 = -INFINITY;
               }
-              mx[e & 3] = fmaxf(mx[e & 3], fmaxf(s0, s1));
-              const float p0 = ex2(fmaf(s0, sl2, nm));
-              const float p1 = ex2(fmaf(s1, sl2, nm));
-              lt[e & 3] += p0 + p1;
-              if (c2 == 0) pk0[e] = pack_bf16x2(p0, p1);
-              else pk1[e] = pack_bf16x2(p0, p1);
+              const float p0 = ex2(x0);
+              const float p1 = ex2(x1);
+              const int a = e & 3;
+              add2(lt[2 * a], lt[2 * a + 1], lt[2 * a], lt[2 * a + 1], p0, p1);
+              const uint32_t w = pack_bf16x2(p0, p1);
+              pmax[a] = max_bf16x2(pmax[a], w);
+              if (c2 == 0) pk0[e] = w;
+              else pk1[e] = w;
             }
           }
-          const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-          exact = __any_sync(0xffffffffu, mraw * sl2 > m + kRescaleThreshold);
+          const uint32_t pm = max_bf16x2(max_bf16x2(pmax[0], pmax[1]), max_bf16x2(pmax[2], pmax[3]));
+          const float pmx = fmaxf(__uint_as_float(pm << 16), __uint_as_float(pm & 0xffff0000u));
+          exact = __any_sync(0xffffffffu, pmx > kGrowthLimit);
           if (!exact) {
-            l += (lt[0] + lt[1]) + (lt[2] + lt[3]);
+            l += ((lt[0] + lt[1]) + (lt[2] + lt[3])) + ((lt[4] + lt[5]) + (lt[6] + lt[7]));
             tmem_st32(s_addr, pk0);
             tmem_st32(s_addr + 32, pk1);
           }

@@ -148,38 +148,51 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(kBlock, kBlock, 0, 0);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(kBlock, D, 0, 1);
-      bool ok = mbar_wait(&sm.bar_q, 0, ab);
-      for (int k = 0; ok && k < ntiles; ++k) {
-        const int s = k & 1;
-        if (!(ok = mbar_wait(&sm.kv_full[s], (k >> 1) & 1, ab))) break;
-        tc_fence_after();
-        const uint32_t kbase = smem_u32(sm.k[s]);
-        for (int t = 0; t < nh && ok; ++t) {
-          if (k > 0) {
-            if (!(ok = mbar_wait(&sm.o_full[t], (k - 1) & 1, ab))) break;
-            tc_fence_after();
-          }
-          const uint32_t qbase = smem_u32(sm.q[t]);
+      auto issue_qk = [&](int t, uint32_t kbase) {
+        const uint32_t qbase = smem_u32(sm.q[t]);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * (kBlock * 128) + (kk & 3) * 32;
-            umma_ss(tbase + t * 128, sdesc_sw128(qbase + off, 16, 1024),
-                    sdesc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0);
-          }
-          umma_commit(&sm.s_full[t]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kBlock * 128) + (kk & 3) * 32;
+          umma_ss(tbase + t * 128, sdesc_sw128(qbase + off, 16, 1024),
+                  sdesc_sw128(kbase + off, 16, 1024), kIdescQK, kk > 0);
         }
-        const uint32_t vbase = smem_u32(sm.v[s]);
+        umma_commit(&sm.s_full[t]);
+      };
+      auto issue_pv = [&](int t, uint32_t vbase, bool accumulate) {
+#pragma unroll
+        for (int kk = 0; kk < kBlock / 16; ++kk)
+          umma_ts(tbase + 256 + t * 128, tbase + t * 128 + kk * 8,
+                  sdesc_sw128(vbase + kk * 2048, kBlock * 128, 1024), kIdescPV,
+                  (accumulate || kk > 0));
+        umma_commit(&sm.o_full[t]);
+      };
+      // Slot by slot: QK_t(k+1) follows PV_t(k) as soon as that completes,
+      // so each head slot runs its own QK -> softmax -> PV cycle and the two
+      // slots settle into an offset schedule that keeps the tensor pipe fed
+      // while the other slot's softmax runs.
+      bool ok = mbar_wait(&sm.bar_q, 0, ab) && mbar_wait(&sm.kv_full[0], 0, ab);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < nh; ++t) issue_qk(t, smem_u32(sm.k[0]));
+      }
+      for (int k = 0; ok && k < ntiles; ++k) {
+        const int s = k & 1, s1 = (k + 1) & 1;
+        const bool more = k + 1 < ntiles;
+        bool next_loaded = false;
         for (int t = 0; t < nh && ok; ++t) {
           if (!(ok = mbar_wait(&sm.p_full[t], k & 1, ab))) break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kBlock / 16; ++kk)
-            umma_ts(tbase + 256 + t * 128, tbase + t * 128 + kk * 8,
-                    sdesc_sw128(vbase + kk * 2048, kBlock * 128, 1024), kIdescPV,
-                    (k > 0 || kk > 0));
-          umma_commit(&sm.o_full[t]);
+          issue_pv(t, smem_u32(sm.v[s]), k > 0);
+          if (t == nh - 1) umma_commit(&sm.kv_empty[s]);   // all PVs of tile k issued
+          if (!more) continue;
+          if (!next_loaded) {
+            if (!(ok = mbar_wait(&sm.kv_full[s1], ((k + 1) >> 1) & 1, ab))) break;
+            next_loaded = true;
+          }
+          if (!(ok = mbar_wait(&sm.o_full[t], k & 1, ab))) break;   // P_t(k) consumed
+          tc_fence_after();
+          issue_qk(t, smem_u32(sm.k[s1]));
         }
-        if (ok) umma_commit(&sm.kv_empty[s]);
       }
       if (!ok) {
         umma_commit(&sm.drain);   // wait for every MMA already issued

@@ -68,7 +68,8 @@ typedef struct CUstream_st* tree_stream_t; /* a cudaStream_t; NULL = legacy defa
 
 typedef enum {
   TREE_OK = 0,
-  TREE_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad head split */
+  TREE_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad head split,
+                                  softmax scale not positive and finite */
   TREE_ERR_ALIGNMENT = 2,      /* T_pad or a capacity not a multiple of 128; unaligned pointer */
   TREE_ERR_CAPACITY = 3,       /* a sequence longer than max_tokens_per_mb */
   TREE_ERR_MALFORMED_TREE = 4, /* token_node/node_entry/node_exit inconsistent (device-detected) */
@@ -195,7 +196,8 @@ TREE_API tree_status_t tree_blockmap_build(const int32_t* key_reach, int32_t T_p
  *   key_reach [in]  device int32[T_pad]
  *   blockmap  [in]  from tree_blockmap_build for the same key_reach
  *   d         [in]  64 or 128; Hq % Hkv == 0
- *   scale     [in]  softmax scale (1/sqrt(d) is the usual choice)
+ *   scale     [in]  softmax scale, positive and finite (1/sqrt(d) is the usual
+ *                   choice); anything else is TREE_ERR_INVALID_ARG
  *   o         [out] device bf16 [T_pad, Hq, d]
  *   lse       [out] device fp32 [Hq, T_pad]
  *   dev_status[out] TREE_ERR_TIMEOUT if a device wait ran out of time
@@ -219,6 +221,7 @@ TREE_API tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v
  * its dK/dV sum over all of them by construction.
  *
  *   o, d_o, lse   [in]  forward output, upstream gradient, forward LSE
+ *   scale         [in]  the forward's scale (positive and finite)
  *   dq            [out] device bf16 [T_pad, Hq, d]
  *   dk, dv        [out] device bf16 [T_pad, Hkv, d]
  *   workspace     [tmp] >= tree_attn_bwd_workspace_bytes(T_pad, Hq, d):

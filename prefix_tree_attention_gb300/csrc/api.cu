@@ -40,6 +40,10 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The softmax scale must be a positive finite number: the kernels take the
+// row max of the raw scores before scaling, which needs scale > 0.
+bool valid_scale(float scale) { return scale > 0.f && scale <= 3.0e38f; }
+
 // The driver's tensor-map encoder, resolved once through the runtime so the
 // library itself does not link libcuda (it loads on machines without a GPU).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -161,6 +165,7 @@ tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v,
                             float* lse, int32_t* dev_status, tree_stream_t stream) {
   tree_status_t st = check_attn_shape(T_pad, Hq, Hkv, d);
   if (st != TREE_OK) return st;
+  if (!valid_scale(scale)) return TREE_ERR_INVALID_ARG;
   if (!dev_status) return TREE_ERR_INVALID_ARG;
   if (T_pad == 0) return TREE_OK;
   if (!q || !k || !v || !key_reach || !blockmap || !o || !lse) return TREE_ERR_INVALID_ARG;
@@ -203,6 +208,7 @@ tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v, co
                                  int32_t* dev_status, tree_stream_t stream) {
   tree_status_t st = check_attn_shape(T_pad, Hq, Hkv, d);
   if (st != TREE_OK) return st;
+  if (!valid_scale(scale)) return TREE_ERR_INVALID_ARG;
   if (!dev_status) return TREE_ERR_INVALID_ARG;
   if (T_pad == 0) return TREE_OK;
   if (!q || !k || !v || !d_o || !key_reach || !blockmap || !dk || !dv || !workspace)
@@ -225,6 +231,7 @@ tree_status_t tree_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float s
                                    int32_t* dev_status, tree_stream_t stream) {
   tree_status_t st = check_attn_shape(T_pad, Hq, 1, d);
   if (st != TREE_OK) return st;
+  if (!valid_scale(scale)) return TREE_ERR_INVALID_ARG;
   if (!dev_status) return TREE_ERR_INVALID_ARG;
   if (T_pad == 0) return TREE_OK;
   if (!workspace || !dq) return TREE_ERR_INVALID_ARG;
@@ -243,6 +250,7 @@ tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v, const v
                             tree_stream_t stream) {
   tree_status_t st = check_attn_shape(T_pad, Hq, Hkv, d);
   if (st != TREE_OK) return st;
+  if (!valid_scale(scale)) return TREE_ERR_INVALID_ARG;
   if (!dev_status) return TREE_ERR_INVALID_ARG;
   if (T_pad == 0) return TREE_OK;
   if (!q || !k || !v || !o || !d_o || !lse || !key_reach || !blockmap || !dq || !dk || !dv ||

@@ -65,6 +65,198 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Visibility bits of the 64 scores c2*64 .. c2*64+63 of a tile for query
+// row i, key j = j0 + column: bit e of vis[w] stands for column
+// c2*64 + 32*w + e and is set when j <= i <= reach[j].  The j <= i part is a
+// prefix of each 32-column group; the reach values are read four at a time
+// (every lane reads the same words, a broadcast).
+__device__ __forceinline__ void visible_bits(const int32_t* rch, int c2, int32_t j0, int32_t i,
+                                             uint32_t (&vis)[2]) {
+  const int4* r4 = reinterpret_cast<const int4*>(rch) + c2 * 16;
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {
+    const int32_t n = i - (j0 + c2 * 64 + w * 32) + 1;   // columns with j <= i
+    const uint32_t pre = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
+    uint32_t rb = 0u;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int4 r = r4[w * 8 + q];
+      rb |= (i <= r.x ? 1u : 0u) << (4 * q);
+      rb |= (i <= r.y ? 1u : 0u) << (4 * q + 1);
+      rb |= (i <= r.z ? 1u : 0u) << (4 * q + 2);
+      rb |= (i <= r.w ? 1u : 0u) << (4 * q + 3);
+    }
+    vis[w] = pre & rb;
+  }
+}
+
+// Largest raw score among the visible columns c2*64 .. c2*64+63 (four
+// independent max chains); -inf when none is visible.
+template <bool kMasked>
+__device__ __forceinline__ float half_max(uint32_t s_addr, int c2, int32_t j0, int32_t i,
+                                          const int32_t* rch) {
+  uint32_t vis[2] = {0xffffffffu, 0xffffffffu};
+  if constexpr (kMasked) visible_bits(rch, c2, j0, i, vis);
+  uint32_t ra[32], rb[32];
+  tmem_ld32x2(s_addr + c2 * 64, s_addr + c2 * 64 + 32, ra, rb);
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int e = 0; e < 64; ++e) {
+    float xv = __uint_as_float(e < 32 ? ra[e] : rb[e - 32]);
+    if constexpr (kMasked) {
+      if (!(vis[e >> 5] & (1u << (e & 31)))) xv = -INFINITY;
+    }
+    mx[e & 3] = fmaxf(mx[e & 3], xv);
+  }
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// Scores c2*64 .. c2*64+63 of a tile against the reference max m (log2
+// units): P = 2^(s*scale*log2e - m) as 32 bf16 pairs in pk, their fp32 sum
+// added to ls.  Paired fp32 math and two independent sum chains.  Returns,
+// warp-uniformly, whether any row of the warp has a score more than the
+// threshold above m, tested on the packed bf16 P itself (P > 2^threshold).
+template <bool kMasked>
+__device__ __forceinline__ bool score_half(uint32_t s_addr, int c2, int32_t j0, int32_t i,
+                                           const int32_t* rch, float sl2, float m,
+                                           uint32_t (&pk)[32], float& ls) {
+  uint32_t vis[2] = {0xffffffffu, 0xffffffffu};
+  if constexpr (kMasked) visible_bits(rch, c2, j0, i, vis);
+  uint32_t ra[32], rb[32];
+  tmem_ld32x2(s_addr + c2 * 64, s_addr + c2 * 64 + 32, ra, rb);
+  float lt[4] = {0.f, 0.f, 0.f, 0.f};
+  uint32_t pmax[2] = {0u, 0u};
+  const float nm = -m;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    float x0, x1;
+    fma2(x0, x1, __uint_as_float(e < 16 ? ra[2 * e] : rb[2 * e - 32]),
+         __uint_as_float(e < 16 ? ra[2 * e + 1] : rb[2 * e - 31]), sl2, sl2, nm, nm);
+    if constexpr (kMasked) {
+      const uint32_t wv = vis[e >> 4];
+      if (!(wv & (1u << ((2 * e) & 31)))) x0 = -INFINITY;
+      if (!(wv & (2u << ((2 * e) & 31)))) x1 = -INFINITY;
+    }
+    const float p0 = ex2(x0);
+    const float p1 = ex2(x1);
+    const int a = e & 1;
+    add2(lt[2 * a], lt[2 * a + 1], lt[2 * a], lt[2 * a + 1], p0, p1);
+    pk[e] = pack_bf16x2(p0, p1);
+    pmax[a] = max_bf16x2(pmax[a], pk[e]);
+  }
+  ls += (lt[0] + lt[1]) + (lt[2] + lt[3]);
+  const uint32_t pm = max_bf16x2(pmax[0], pmax[1]);
+  const float pmx = fmaxf(__uint_as_float(pm << 16), __uint_as_float(pm & 0xffff0000u));
+  return __any_sync(0xffffffffu, pmx > kGrowthLimit);
+}
+
+// O *= alpha (per row) in TMEM; warp-collective.
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t o_addr, float alpha) {
+#pragma unroll
+  for (int c4 = 0; c4 < D / 32; ++c4) {
+    uint32_t reg[32];
+    tmem_ld32(o_addr + c4 * 32, reg);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) reg[e] = __float_as_uint(__uint_as_float(reg[e]) * alpha);
+    tmem_st32(o_addr + c4 * 32, reg);
+  }
+}
+
+// Rare case: some row's max grew past the threshold within the second half
+// of a tile after the first half's P had already been written over S.  The
+// new reference max is the old one plus a whole number n of log2 units, so
+// the stored first-half P (bf16) and O scale by the exact power of two 2^-n;
+// the second half is recomputed from its scores, still intact in TMEM.
+// Warp-collective: every TMEM access runs for the whole warp, with scale 1
+// on the rows that did not grow.
+template <int D, bool kMasked>
+__device__ __forceinline__ void late_growth(uint32_t s_addr, uint32_t o_addr, int32_t j0, int32_t i,
+                                            const int32_t* rch, float sl2, bool has_o, float& m,
+                                            float& l, float ls0) {
+  tmem_st_wait();   // the first-half P store must land before it is read back
+  const float mt = half_max<kMasked>(s_addr, 1, j0, i, rch) * sl2;
+  const bool grow = mt > m + kRescaleThreshold;
+  const int n = grow ? static_cast<int>(ceilf(mt - m)) : 0;
+  const float alpha = n > 125 ? 0.f : __int_as_float((127 - n) << 23);   // 2^-n
+  m += static_cast<float>(n);
+  l = (l + ls0) * alpha;
+  if (__any_sync(0xffffffffu, grow)) {
+    if (has_o) rescale_o<D>(o_addr, alpha);
+    uint32_t pk[32];
+    tmem_ld32(s_addr, pk);
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      pk[e] = pack_bf16x2(__uint_as_float(pk[e] << 16) * alpha,
+                          __uint_as_float(pk[e] & 0xffff0000u) * alpha);
+    tmem_st32(s_addr, pk);
+  }
+  uint32_t pk[32];
+  float ls1 = 0.f;
+  score_half<kMasked>(s_addr, 1, j0, i, rch, sl2, m, pk, ls1);   // now within the threshold
+  tmem_st32(s_addr + 32, pk);
+  l += ls1;
+}
+
+// One key tile of the online softmax for the query row held in this thread's
+// TMEM lane: reads S (128 fp32 columns at s_addr), writes P as bf16 pairs over
+// its first 64 columns, updates the running max m (log2 units) and sum l, and
+// rescales O (at o_addr) in the rare case the max grew past the threshold.
+// kMasked is a template argument so that FULL tiles run without the
+// visibility test.
+template <int D, bool kMasked>
+__device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, int32_t j0,
+                                             int32_t i, const int32_t* rch, float sl2,
+                                             bool has_o, float& m, float& l) {
+  uint32_t pk[32];
+  // Common path: one pass per 64-column half against the running max of the
+  // earlier tiles (one FMA + ex2 per score).  Half 0's P goes over columns
+  // 0..31 once its 64 scores are in registers and no row grew past the
+  // threshold; half 1's P over columns 32..63.  Growth in half 0 leaves S
+  // intact for the exact path below; growth in half 1 goes to late_growth.
+  // Rows with no running max yet (a row's first visible tile) always take
+  // the exact path.
+  if (!__any_sync(0xffffffffu, m == -INFINITY)) {
+    float ls0 = 0.f;
+    if (!score_half<kMasked>(s_addr, 0, j0, i, rch, sl2, m, pk, ls0)) {
+      tmem_st32(s_addr, pk);
+      float ls1 = 0.f;
+      if (!score_half<kMasked>(s_addr, 1, j0, i, rch, sl2, m, pk, ls1)) {
+        tmem_st32(s_addr + 32, pk);
+        l += ls0 + ls1;
+      } else {
+        late_growth<D, kMasked>(s_addr, o_addr, j0, i, rch, sl2, has_o, m, l, ls0);
+      }
+      return;
+    }
+  }
+  // Exact path: the tile's row max first, then the same two half passes
+  // against the updated reference.  The decision is per row, but tcgen05
+  // loads and stores are warp-collective: O is rescaled for the whole warp
+  // when any of its rows needs it, with alpha = 1 on the rows that do not.
+  // (A row whose earlier tiles were all masked, e.g. one past a top-level
+  // subtree boundary inside the block, first sees a key at a later tile.)
+  const float mt = fmaxf(half_max<kMasked>(s_addr, 0, j0, i, rch),
+                         half_max<kMasked>(s_addr, 1, j0, i, rch)) * sl2;
+  const float mnew = fmaxf(m, mt);
+  const bool grow = mnew > m + kRescaleThreshold;
+  const float alpha = grow ? ex2(m - mnew) : 1.f;   // 0 when m = -inf
+  if (grow) {
+    l *= alpha;
+    m = mnew;
+  }
+  if (has_o && __any_sync(0xffffffffu, grow)) rescale_o<D>(o_addr, alpha);
+  // A row with nothing visible so far keeps m = -inf; its scores are all
+  // masked here, so any finite reference gives P = 0.
+  const float mref = (m == -INFINITY) ? 0.f : m;
+  float ls = 0.f;
+  score_half<kMasked>(s_addr, 0, j0, i, rch, sl2, mref, pk, ls);
+  tmem_st32(s_addr, pk);
+  score_half<kMasked>(s_addr, 1, j0, i, rch, sl2, mref, pk, ls);
+  tmem_st32(s_addr + 32, pk);
+  l += ls;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -219,122 +411,11 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (k + 1 < ntiles) kb_next = tiles[k + 1];
         if (!(ok = mbar_wait_warp(&sm.s_full[t], k & 1, ab))) break;
         tc_fence_after();
-        const bool partial = k >= nfull;
         const int32_t* rch = sm.reach[k & 1];
-        const float sl2 = p.scale_log2;
-        // Common path: one pass against the running max of the earlier tiles
-        // (p = 2^(s*scale*log2e - m) in one FMA + ex2).  P stays in
-        // registers and is written over S only when no row's max grew by
-        // more than the threshold; otherwise S is still intact and the exact
-        // two-pass path below redoes the tile.  Rows with no running max yet
-        // (a row's first visible tile) always take the exact path.
-        bool exact = __any_sync(0xffffffffu, m == -INFINITY);
-        if (!exact) {
-          uint32_t pk0[32], pk1[32];
-          // Paired fp32 math, four independent sum chains, and the growth
-          // test on the packed bf16 P itself: P > 2^threshold exactly when
-          // the score exceeds the running max by more than the threshold.
-          float lt[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          uint32_t pmax[4] = {0u, 0u, 0u, 0u};
-          const float nm = -m;
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t ra[32], rb[32];
-            tmem_ld32x2(s_addr + c2 * 64, s_addr + c2 * 64 + 32, ra, rb);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int c = c2 * 64 + 2 * e;
-              float x0, x1;
-              fma2(x0, x1, __uint_as_float(e < 16 ? ra[2 * e] : rb[2 * e - 32]),
-                   __uint_as_float(e < 16 ? ra[2 * e + 1] : rb[2 * e - 31]), sl2, sl2, nm, nm);
-              if (partial) {
-                if (!((j0 + c <= i) && (i <= rch[c]))) x0 = -INFINITY;
-                if (!((j0 + c + 1 <= i) && (i <= rch[c + 1]))) x1 = -INFINITY;
-              }
-              const float p0 = ex2(x0);
-              const float p1 = ex2(x1);
-              const int a = e & 3;
-              add2(lt[2 * a], lt[2 * a + 1], lt[2 * a], lt[2 * a + 1], p0, p1);
-              const uint32_t w = pack_bf16x2(p0, p1);
-              pmax[a] = max_bf16x2(pmax[a], w);
-              if (c2 == 0) pk0[e] = w;
-              else pk1[e] = w;
-            }
-          }
-          const uint32_t pm = max_bf16x2(max_bf16x2(pmax[0], pmax[1]), max_bf16x2(pmax[2], pmax[3]));
-          const float pmx = fmaxf(__uint_as_float(pm << 16), __uint_as_float(pm & 0xffff0000u));
-          exact = __any_sync(0xffffffffu, pmx > kGrowthLimit);
-          if (!exact) {
-            l += ((lt[0] + lt[1]) + (lt[2] + lt[3])) + ((lt[4] + lt[5]) + (lt[6] + lt[7]));
-            tmem_st32(s_addr, pk0);
-            tmem_st32(s_addr + 32, pk1);
-          }
-        }
-        if (exact) {
-        // Exact path: pass 1 finds the row max, pass 2 reloads, exponentiates
-        // and packs.
-        float mt = -INFINITY;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; c4 += 2) {
-          uint32_t ra[32], rb[32];
-          tmem_ld32x2(s_addr + c4 * 32, s_addr + c4 * 32 + 32, ra, rb);
-#pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const int c = c4 * 32 + e;
-            float xv = __uint_as_float(e < 32 ? ra[e] : rb[e - 32]) * p.scale_log2;
-            if (partial && !((j0 + c <= i) && (i <= rch[c]))) xv = -INFINITY;
-            mt = fmaxf(mt, xv);
-          }
-        }
-        const float mnew = fmaxf(m, mt);
-        // The decision is per row, but tcgen05.ld/st are warp-collective: the
-        // O rescale runs for the whole warp when any of its rows needs it,
-        // with alpha = 1 on the rows that do not.  (A row whose earlier tiles
-        // were all masked, e.g. one past a top-level subtree boundary inside
-        // the block, first sees a key at a later tile.)
-        const bool grow = mnew > m + kRescaleThreshold;
-        const float alpha = grow ? ex2(m - mnew) : 1.f;   // 0 when m = -inf
-        if (grow) {
-          l *= alpha;
-          m = mnew;
-        }
-        if (k > 0 && __any_sync(0xffffffffu, grow)) {
-#pragma unroll
-          for (int c4 = 0; c4 < D / 32; ++c4) {
-            uint32_t reg[32];
-            tmem_ld32(o_addr + c4 * 32, reg);
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              reg[e] = __float_as_uint(__uint_as_float(reg[e]) * alpha);
-            tmem_st32(o_addr + c4 * 32, reg);
-          }
-        }
-        const float msub = (m == -INFINITY) ? 0.f : m;
-        // Columns c2*64 .. c2*64+63 are read before their packed P words are
-        // written to columns c2*32 .. c2*32+31, so no unread score is lost.
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t ra[32], rb[32], pk[32];
-          tmem_ld32x2(s_addr + c2 * 64, s_addr + c2 * 64 + 32, ra, rb);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int c = c2 * 64 + 2 * e;
-            const uint32_t* src = e < 16 ? ra : rb;
-            const int off = (e < 16 ? 2 * e : 2 * e - 32);
-            float x0 = __uint_as_float(src[off]) * p.scale_log2;
-            float x1 = __uint_as_float(src[off + 1]) * p.scale_log2;
-            if (partial) {
-              if (!((j0 + c <= i) && (i <= rch[c]))) x0 = -INFINITY;
-              if (!((j0 + c + 1 <= i) && (i <= rch[c + 1]))) x1 = -INFINITY;
-            }
-            const float p0 = ex2(x0 - msub);
-            const float p1 = ex2(x1 - msub);
-            l += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
-          }
-          tmem_st32(s_addr + c2 * 32, pk);
-        }
-        }   // exact path
+        if (k >= nfull)
+          softmax_tile<D, true>(s_addr, o_addr, j0, i, rch, p.scale_log2, k > 0, m, l);
+        else
+          softmax_tile<D, false>(s_addr, o_addr, j0, i, rch, p.scale_log2, k > 0, m, l);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full[t]);

@@ -67,6 +67,10 @@ def test_host_side_errors_return_before_launch():
     assert f(*args(256, 4, 4, 64, q=None)) == 1  # null pointer
     assert f(*args(256, 4, 4, 64, q=FAKE + 4)) == 2  # unaligned pointer
     assert f(*args(0, 4, 4, 64)) == 0            # empty input is a no-op
+    for bad in (0.0, -0.1, float("nan"), float("inf")):   # scale not positive and finite
+        a = list(args(256, 4, 4, 64))
+        a[9] = bad
+        assert f(*a) == 1, bad
     b = lib.tree_blockmap_build
     b.restype = ctypes.c_int
     b.argtypes = [P, ctypes.c_int32, ctypes.c_int32, P, ctypes.c_size_t, P, P]
@@ -84,6 +88,8 @@ def test_host_side_errors_return_before_launch():
     bw.argtypes = [P] * 8 + [ctypes.c_int32] * 4 + [ctypes.c_float] + [P] * 4 + \
         [ctypes.c_size_t, P, P]
     assert bw(*([FAKE] * 8), 256, 8, 2, 128, 0.1, FAKE, FAKE, FAKE, FAKE, 64, FAKE, None) == 8
+    assert bw(*([FAKE] * 8), 256, 8, 2, 128, -1.0, FAKE, FAKE, FAKE, FAKE, 1 << 30, FAKE,
+              None) == 1
 
 
 def _same_packing(mine, ref):

@@ -120,6 +120,18 @@ def half_ulp_bf16(x):
     return np.where(a > 0, np.exp2(e - 8), 0.0)
 
 
+def stored_o(o_ref):
+    """The forward output as the backward receives it: rounded to bf16.
+
+    The backward's D = rowsum(dO * O) term is a function of the O it is
+    given, so the reference backward is evaluated at the oracle's own O
+    rounded to bf16 (round to nearest even), not at the exact O.  With keys
+    of large norm the two differ visibly: a row dominated by one key has
+    dP - D close to zero, and the rounding of O moves D by up to ~0.2.
+    """
+    return torch.from_numpy(o_ref).to(torch.bfloat16).double().numpy()
+
+
 def max_bound(want):
     return MAX_ERR + half_ulp_bf16(want)
 
@@ -132,16 +144,16 @@ def assert_close(name, got, want, real):
     assert err.mean() <= MEAN_ERR, f"{name}: mean err {err.mean():.3e}"
 
 
-def check_attention_dense(packed, Hq, Hkv, d, seed=0):
+def check_attention_dense(packed, Hq, Hkv, d, seed=0, tensors=None):
     T = packed.T_pad
-    t = W.tensors(T, Hq, Hkv, d, seed=seed, device=DEV)
+    t = tensors if tensors is not None else W.tensors(T, Hq, Hkv, d, seed=seed, device=DEV)
     bufs = run_positions_blockmap(packed.token_node, packed.node_entry, packed.node_exit)
     o, lse, dq, dk, dv = run_attention(bufs, t["q"], t["k"], t["v"], t["do"])
     q, k, v, do = (_f64(t[n]) for n in ("q", "k", "v", "do"))
     M = OM.ancestor_mask(packed)
     scale = d ** -0.5
     o_ref, lse_ref = OA.forward(q, k, v, M, scale)
-    dq_ref, dk_ref, dv_ref = OA.backward(q, k, v, o_ref, do, M, scale)
+    dq_ref, dk_ref, dv_ref = OA.backward(q, k, v, stored_o(o_ref), do, M, scale)
     real = packed.token_node >= 0
     pad = ~real
     assert_close("O", _f64(o), o_ref, real)
@@ -275,6 +287,69 @@ def test_full_tiles_long_prefix():
     assert (OM.tile_classes(p) == 1).sum() > 10
     bufs = check_attention_dense(p, 4, 2, 128, seed=2)
     check_integer_outputs(p, bufs)
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(4, 2, 128), (2, 1, 64)])
+def test_score_jumps_force_rescale(Hq, Hkv, d):
+    # Every query shares the all-ones direction and a few keys point along
+    # it, so rows that see those keys have their running max jump by about
+    # 17, 24, 33, 140 and 33 log2 units at later tiles: in the first and in
+    # the second 64-column half of a tile, in FULL and PARTIAL tiles, and once
+    # by so much that the earlier terms underflow to zero.  This drives the
+    # forward's O and P rescale paths, which random scores never reach.
+    rng = W.SplitMix64(21)
+    prefix = [rng.randint(1, 50) for _ in range(900)]
+    seqs = [prefix + [100 + i] * rng.randint(100, 700) for i in range(4)]
+    _, (p,) = pack_both(seqs, 4096)
+    T = p.T_pad
+    t = W.tensors(T, Hq, Hkv, d, seed=3, device=DEV)
+    g = (128 / d) ** 0.5
+    k = t["k"].clone()
+    for j, beta in ((200, 1.5), (300, 2.5), (650, 3.5), (870, 12.0), (1000, 14.0)):
+        k[j] = beta * g
+    t = dict(t, q=(t["q"].float() + 1.0).to(torch.bfloat16), k=k)
+    bufs = run_positions_blockmap(p.token_node, p.node_entry, p.node_exit)
+    check_integer_outputs(p, bufs)
+    o, lse, _, _, _ = run_attention(bufs, t["q"], t["k"], t["v"], t["do"])
+    q, k, v, do = (_f64(t[n]) for n in ("q", "k", "v", "do"))
+    M = OM.ancestor_mask(p)
+    scale = d ** -0.5
+    o_ref, lse_ref = OA.forward(q, k, v, M, scale)
+    real = p.token_node >= 0
+    assert_close("O", _f64(o), o_ref, real)
+    assert np.abs(lse.cpu().numpy()[:, real] - lse_ref[:, real]).max() <= LSE_ERR
+    # The backward on its own, at the oracle's O (rounded to bf16, as the
+    # forward stores it) and LSE: with keys this large, D = rowsum(dO * O)
+    # is sensitive to the last bit of O.
+    o_in = torch.from_numpy(stored_o(o_ref)).to(torch.bfloat16).to(DEV)
+    lse_in = torch.from_numpy(lse_ref).float().to(DEV)
+    dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+    ws = torch.empty((ptg.attn_bwd_workspace_bytes(T, Hq, d) + 3) // 4, dtype=torch.float32,
+                     device=DEV)
+    ptg.tree_attn_bwd(t["q"], t["k"], t["v"], o_in, t["do"], lse_in, bufs.key_reach,
+                      bufs.blockmap, dq, dk, dv, ws, bufs.status)
+    torch.cuda.synchronize()
+    assert int(bufs.status.item()) == 0
+    o_st = stored_o(o_ref)
+    dq_ref, dk_ref, dv_ref = OA.backward(q, k, v, o_st, do, M, scale)
+    assert_close("dV", _f64(dv), dv_ref, real)
+    # dQ and dK take dS rounded to bf16 (relative error <= 2^-9) times keys
+    # and queries of norm up to 14*sqrt(d): allow one bf16 ulp of dS on
+    # every term of their sums on top of the usual bound.
+    bq, bk = np.zeros_like(dq_ref), np.zeros_like(dk_ref)
+    g_ = Hq // Hkv
+    for h in range(Hq):
+        hk = h // g_
+        S = np.where(M, q[:, h] @ k[:, hk].T * scale, -np.inf)
+        P = np.exp(S - np.where(np.isfinite(lse_ref[h]), lse_ref[h], 0.0)[:, None])
+        dS = np.abs(P * (do[:, h] @ v[:, hk].T - (do[:, h] * o_st[:, h]).sum(1)[:, None]))
+        bq[:, h] = 2.0 ** -8 * scale * dS @ np.abs(k[:, hk])
+        bk[:, hk] += 2.0 ** -8 * scale * dS.T @ np.abs(q[:, h])
+    for name, got, want, extra in (("dQ", dq, dq_ref, bq), ("dK", dk, dk_ref, bk)):
+        err = np.abs(_f64(got)[real] - want[real])
+        excess = err - max_bound(want[real]) - extra[real]
+        assert excess.max() <= 0, f"{name}: max err {err.max():.3e}, excess {excess.max():.3e}"
+        assert err.mean() <= MEAN_ERR, f"{name}: mean err {err.mean():.3e}"
 
 
 def test_forest_of_two_tries_in_one_buffer():

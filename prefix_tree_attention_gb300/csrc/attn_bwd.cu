@@ -73,6 +73,35 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Adds a warp's 32 rows x 32 fp32 columns (lane = row, v = that row's 32
+// values) to dst[row * row_stride + 0..31] with red.global.add.v4, staged
+// through 4 KB of shared scratch: each lane writes its row as eight 16-byte
+// chunks XOR-swizzled by row (conflict-free), then 8 lanes read one row's
+// 128 contiguous bytes, so each red instruction of the warp covers four
+// whole 128-byte lines instead of 32 half-filled 32-byte sectors.
+__device__ __forceinline__ void red_rows_coalesced(uint8_t* scratch, const uint32_t (&v)[32],
+                                                   float* dst, uint32_t row_stride, int lane) {
+  __syncwarp();
+  uint8_t* mine = scratch + lane * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(mine + ((c ^ (lane & 7)) << 4)) =
+        make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+  __syncwarp();
+  const int sub = lane & 7;
+  // 32-bit offsets from dst: a dQ accumulator spans far less than 2^32 floats.
+  uint32_t off = static_cast<uint32_t>(lane >> 3) * row_stride + sub * 4;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int row = it * 4 + (lane >> 3);
+    const uint4 x = *reinterpret_cast<const uint4*>(scratch + row * 128 + ((sub ^ (row & 7)) << 4));
+    red_add_v4(dst + off, __uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
+               __uint_as_float(x.w));
+    off += 4 * row_stride;
+  }
+  __syncwarp();
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -321,31 +350,29 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       // dQ rows (TMEM lane = query row), columns w*D/2 .. of this head.
       if (!(ok = mbar_wait_warp(&sm.dq_full, n & 1, ab))) break;
       tc_fence_after();
-      float* dst = p.dq_acc + (static_cast<size_t>(qa * kBlock + r) * p.Hq + h) * D + w * (D / 2);
+      // The warp's dQ rows go out through its own 4 KB of the dS tile (the
+      // dQ MMA that read it has completed; the warp rewrites it only with the
+      // next dS) so that the fp32 adds are whole 128-byte lines.
+      uint8_t* scratch =
+          reinterpret_cast<uint8_t*>(sm.ds) + w * (kBlock * 128) + quarter * 32 * 128;
+      float* dst = p.dq_acc + (static_cast<size_t>(qa * kBlock + quarter * 32) * p.Hq + h) * D +
+                   w * (D / 2);
+      const uint32_t row_stride = static_cast<uint32_t>(p.Hq) * D;
       const uint32_t dq_col = tbase + lane_off + kDQ + w * (D / 2);
       if constexpr (D == 128) {
-        uint32_t ra[32], rb[32];
-        tmem_ld32x2(dq_col, dq_col + 32, ra, rb);
+        uint32_t ra[32];
+        tmem_ld32(dq_col, ra);
+        red_rows_coalesced(scratch, ra, dst, row_stride, lane);
+        tmem_ld32(dq_col + 32, ra);
         tc_fence_before();
         mbar_arrive(&sm.dq_free);     // TMEM read done; the adds below need only registers
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          red_add_v4(dst + 4 * e, __uint_as_float(ra[4 * e]), __uint_as_float(ra[4 * e + 1]),
-                     __uint_as_float(ra[4 * e + 2]), __uint_as_float(ra[4 * e + 3]));
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          red_add_v4(dst + 32 + 4 * e, __uint_as_float(rb[4 * e]),
-                     __uint_as_float(rb[4 * e + 1]), __uint_as_float(rb[4 * e + 2]),
-                     __uint_as_float(rb[4 * e + 3]));
+        red_rows_coalesced(scratch, ra, dst + 32, row_stride, lane);
       } else {
         uint32_t ra[32];
         tmem_ld32(dq_col, ra);
         tc_fence_before();
         mbar_arrive(&sm.dq_free);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          red_add_v4(dst + 4 * e, __uint_as_float(ra[4 * e]), __uint_as_float(ra[4 * e + 1]),
-                     __uint_as_float(ra[4 * e + 2]), __uint_as_float(ra[4 * e + 3]));
+        red_rows_coalesced(scratch, ra, dst, row_stride, lane);
       }
     }
     // ---------------------------------------------------------- epilogue

@@ -22,9 +22,10 @@ cudaError_t launch_attn_bwd_prepare(const void* o, const void* d_o, const float*
                                     int32_t* status, cudaStream_t s, int num_sms);
 cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo,
-                                 const int32_t* key_reach, const void* blockmap, int32_t T_pad,
-                                 int32_t Hq, int32_t Hkv, int32_t d, float scale, void* dk,
-                                 void* dv, void* workspace, int32_t* status, cudaStream_t s);
+                                 const CUtensorMap& tdq, const int32_t* key_reach,
+                                 const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
+                                 int32_t d, float scale, void* dk, void* dv, void* workspace,
+                                 int32_t* status, cudaStream_t s);
 cudaError_t launch_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
                                    void* workspace, void* dq, int32_t* status, cudaStream_t s,
                                    int num_sms);
@@ -76,6 +77,23 @@ bool encode_map(CUtensorMap* map, const void* base, int32_t T, int32_t H, int32_
                                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The fp32 dQ accumulator [T, H, d] as a 3-D TMA map for reduce-add stores:
+// 32-float (128-byte) x 1 head x 32-token box, 128-byte swizzle.
+bool encode_map_acc(CUtensorMap* map, void* base, int32_t T, int32_t H, int32_t d) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                           static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(d) * 4};
+  cuuint32_t box[3] = {32, 1, 32};
+  cuuint32_t elem[3] = {1, 1, 1};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, elem,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -217,12 +235,13 @@ tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v, co
   for (const void* p : ptrs)
     if (!aligned16(p)) return TREE_ERR_ALIGNMENT;
   if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
-      !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&tdo, d_o, T_pad, Hq, d))
+      !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&tdo, d_o, T_pad, Hq, d) ||
+      !encode_map_acc(&tdq, workspace, T_pad, Hq, d))   // the accumulator leads the workspace
     return TREE_ERR_CUDA;
-  return cuda_result(tree::launch_attn_bwd_main(tq, tk, tv, tdo, key_reach, blockmap, T_pad, Hq,
-                                                Hkv, d, scale, dk, dv, workspace, dev_status,
+  return cuda_result(tree::launch_attn_bwd_main(tq, tk, tv, tdo, tdq, key_reach, blockmap, T_pad,
+                                                Hq, Hkv, d, scale, dk, dv, workspace, dev_status,
                                                 stream));
 }
 

@@ -73,33 +73,28 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Adds a warp's 32 rows x 32 fp32 columns (lane = row, v = that row's 32
-// values) to dst[row * row_stride + 0..31] with red.global.add.v4, staged
-// through 4 KB of shared scratch: each lane writes its row as eight 16-byte
-// chunks XOR-swizzled by row (conflict-free), then 8 lanes read one row's
-// 128 contiguous bytes, so each red instruction of the warp covers four
-// whole 128-byte lines instead of 32 half-filled 32-byte sectors.
-__device__ __forceinline__ void red_rows_coalesced(uint8_t* scratch, const uint32_t (&v)[32],
-                                                   float* dst, uint32_t row_stride, int lane) {
+// Stages a warp's 32 rows x 32 fp32 columns (lane = row, v = that row's 32
+// values) in 4 KB of shared memory in the layout of a 128-byte-swizzled TMA
+// box (row r's 16-byte chunk c at (c ^ (r & 7)) * 16, conflict-free), then
+// lane 0 adds the box into the dQ accumulator with one bulk tensor
+// reduce-add at (column x, head h, token row).  Before the scratch is
+// rewritten, lane 0 waits for the previous reduce to have read it.
+__device__ __forceinline__ void reduce_rows_tma(uint8_t* scratch, const uint32_t (&v)[32],
+                                                const CUtensorMap* map, int x, int h, int row,
+                                                int lane) {
+  if (lane == 0) bulk_wait_read();
   __syncwarp();
   uint8_t* mine = scratch + lane * 128;
 #pragma unroll
   for (int c = 0; c < 8; ++c)
     *reinterpret_cast<uint4*>(mine + ((c ^ (lane & 7)) << 4)) =
         make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+  fence_proxy_async_smem();   // generic-proxy writes -> visible to the bulk copy
   __syncwarp();
-  const int sub = lane & 7;
-  // 32-bit offsets from dst: a dQ accumulator spans far less than 2^32 floats.
-  uint32_t off = static_cast<uint32_t>(lane >> 3) * row_stride + sub * 4;
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int row = it * 4 + (lane >> 3);
-    const uint4 x = *reinterpret_cast<const uint4*>(scratch + row * 128 + ((sub ^ (row & 7)) << 4));
-    red_add_v4(dst + off, __uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
-               __uint_as_float(x.w));
-    off += 4 * row_stride;
+  if (lane == 0) {
+    tma_reduce_add_3d(map, scratch, x, h, row);
+    bulk_commit();
   }
-  __syncwarp();
 }
 
 template <int D>
@@ -107,7 +102,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                     const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   if (ld_status(p.status)) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {          // the layout needs 1024-byte alignment
@@ -336,6 +332,10 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_st32(tbase + lane_off + kS + w * 64, pk);
       tmem_st32(tbase + lane_off + kS + w * 64 + 32, dsw);
       // dS^T row r, queries w*64 .. w*64+63 -> swizzled [key][query] half w.
+      // These 4 KB also stage this warp's dQ rows: the previous step's
+      // reduce must have read them first.
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
       {
         uint8_t* row = reinterpret_cast<uint8_t*>(sm.ds) + w * (kBlock * 128) + r * 128;
 #pragma unroll
@@ -352,29 +352,30 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       tc_fence_after();
       // The warp's dQ rows go out through its own 4 KB of the dS tile (the
       // dQ MMA that read it has completed; the warp rewrites it only with the
-      // next dS) so that the fp32 adds are whole 128-byte lines.
+      // next dS, after the reduce has read it) as bulk tensor reduce-adds.
       uint8_t* scratch =
           reinterpret_cast<uint8_t*>(sm.ds) + w * (kBlock * 128) + quarter * 32 * 128;
-      float* dst = p.dq_acc + (static_cast<size_t>(qa * kBlock + quarter * 32) * p.Hq + h) * D +
-                   w * (D / 2);
-      const uint32_t row_stride = static_cast<uint32_t>(p.Hq) * D;
+      const int row0 = qa * kBlock + quarter * 32;
       const uint32_t dq_col = tbase + lane_off + kDQ + w * (D / 2);
       if constexpr (D == 128) {
-        uint32_t ra[32];
-        tmem_ld32(dq_col, ra);
-        red_rows_coalesced(scratch, ra, dst, row_stride, lane);
-        tmem_ld32(dq_col + 32, ra);
+        uint32_t ra[32], rb[32];
+        tmem_ld32x2(dq_col, dq_col + 32, ra, rb);
         tc_fence_before();
         mbar_arrive(&sm.dq_free);     // TMEM read done; the adds below need only registers
-        red_rows_coalesced(scratch, ra, dst + 32, row_stride, lane);
+        reduce_rows_tma(scratch, ra, &tm_dq, w * 64, h, row0, lane);
+        reduce_rows_tma(scratch, rb, &tm_dq, w * 64 + 32, h, row0, lane);
       } else {
         uint32_t ra[32];
         tmem_ld32(dq_col, ra);
         tc_fence_before();
         mbar_arrive(&sm.dq_free);
-        red_rows_coalesced(scratch, ra, dst, row_stride, lane);
+        reduce_rows_tma(scratch, ra, &tm_dq, w * 32, h, row0, lane);
       }
     }
+    // The last reduces must have read the scratch before the CTA exits, and
+    // have landed before a later kernel reads the accumulator.
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     // ---------------------------------------------------------- epilogue
     __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(jkey) * p.Hkv + kvh) * D + w * (D / 2);
     __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(jkey) * p.Hkv + kvh) * D + w * (D / 2);
@@ -513,9 +514,10 @@ cudaError_t launch_attn_bwd_prepare(const void* o, const void* d_o, const float*
 
 cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo,
-                                 const int32_t* key_reach, const void* blockmap, int32_t T_pad,
-                                 int32_t Hq, int32_t Hkv, int32_t d, float scale, void* dk,
-                                 void* dv, void* workspace, int32_t* status, cudaStream_t s) {
+                                 const CUtensorMap& tdq, const int32_t* key_reach,
+                                 const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
+                                 int32_t d, float scale, void* dk, void* dv, void* workspace,
+                                 int32_t* status, cudaStream_t s) {
   BwdWorkspace w = carve(workspace, T_pad, Hq, d);
   BwdParams p;
   p.key_reach = key_reach;
@@ -539,13 +541,15 @@ cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(BwdSmem<64>)));
     if (e != cudaSuccess) return e;
-    tree_attn_bwd_kernel<64><<<grid, kBwdThreads, sizeof(BwdSmem<64>), s>>>(tq, tk, tv, tdo, p);
+    tree_attn_bwd_kernel<64><<<grid, kBwdThreads, sizeof(BwdSmem<64>), s>>>(tq, tk, tv, tdo, tdq,
+                                                                          p);
   } else {
     e = cudaFuncSetAttribute(tree_attn_bwd_kernel<128>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(BwdSmem<128>)));
     if (e != cudaSuccess) return e;
-    tree_attn_bwd_kernel<128><<<grid, kBwdThreads, sizeof(BwdSmem<128>), s>>>(tq, tk, tv, tdo, p);
+    tree_attn_bwd_kernel<128><<<grid, kBwdThreads, sizeof(BwdSmem<128>), s>>>(tq, tk, tv, tdo,
+                                                                            tdq, p);
   }
   count_launches(1);
   return cudaGetLastError();

@@ -57,15 +57,16 @@ def source_hash(path: str) -> str:
 
 
 def recorded_traffic():
-    """Per-launch DRAM bytes of the bwd main kernel from a committed ncu
-    summary, or None when absent or taken on a different kernel source."""
+    """DRAM bytes of the bwd main kernel over one step of the default
+    workload (all its launches), from a committed ncu summary; None when
+    absent or taken on a different kernel source."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     with open(PROFILE_TRAFFIC) as f:
         rec = json.load(f)
     if rec.get("kernel_source_sha256_16") != source_hash(KERNEL_SOURCE):
         return None
-    return rec.get("bytes_per_launch_full_workload")
+    return rec.get("dram_bytes_per_step")
 
 
 class ClockSampler:

@@ -68,7 +68,7 @@ def test_clock_summary_parses_samples():
 
 
 def test_recorded_traffic_is_null_when_source_changed(tmp_path, monkeypatch):
-    rec = {"kernel_source_sha256_16": "0" * 16, "bytes_per_launch_full_workload": 123}
+    rec = {"kernel_source_sha256_16": "0" * 16, "dram_bytes_per_step": 123}
     p = tmp_path / "t.json"
     p.write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(p))

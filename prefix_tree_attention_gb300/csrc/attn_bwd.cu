@@ -24,9 +24,21 @@
 //                dQ   = dS K             SS (dS staged in smem, MN-major)
 //                                        -> TMEM [384, 384+d), then fp32
 //                                        vector atomics into the accumulator.
-//              warp 0: TMA producer (K, V once; Q, dO, lse2, D per pair in a
-//              2-stage ring); warp 1: TMEM allocator + MMA issuer; warps 2-5
-//              and 6-9: element-wise work on query columns 0-63 and 64-127.
+//              Sixteen warps in four warpgroups:
+//                warps 0-3   dQ warpgroup: per pair, dQ out of TMEM, staged in
+//                            the smem dS tile (free once the dQ MMA has read
+//                            it) and added into the fp32 accumulator by bulk
+//                            tensor reduce-adds at L2;
+//                warps 4-11  element-wise warps (P, dS) on query columns 0-63
+//                            and 64-127;
+//                warp 12     TMA producer (K, V once; Q, dO, lse2, D per pair in
+//                            a 2-stage ring);
+//                warp 13     TMEM allocator + MMA issuer; warps 14-15 idle.
+//              The element-wise warps never wait for a bulk copy: only their
+//              next dS store waits until the dQ warps' reduces have read the
+//              tile, so every element-wise warp reaches the next pair at the
+//              same time.  setmaxnreg moves registers from the control and dQ
+//              warpgroups to the element-wise ones.
 //  a6 convert  dQ = bf16(scale * accumulator).
 #include <cuda_bf16.h>
 
@@ -36,7 +48,12 @@
 namespace tree {
 namespace {
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 512;
+// Per-thread registers after the split (launch: 512 x 128).
+constexpr uint32_t kRegsDq = 96, kRegsEw = 168, kRegsCtl = 72;
+static_assert(128 * kRegsDq + 256 * kRegsEw + 128 * kRegsCtl <= kBwdThreads * 128,
+              "register split exceeds the launch allocation");
+constexpr int kWarpProducer = 12, kWarpMma = 13, kWarpEw0 = 4;
 
 template <int D>
 struct __align__(1024) BwdSmem {
@@ -44,12 +61,13 @@ struct __align__(1024) BwdSmem {
   __nv_bfloat16 v[kBlock * D];
   __nv_bfloat16 q[2][kBlock * D];       // ring stages
   __nv_bfloat16 dout[2][kBlock * D];
-  __nv_bfloat16 ds[kBlock * kBlock];    // dS^T as [key][query], two 64-query halves
+  __nv_bfloat16 ds[kBlock * kBlock];    // dS^T as [key][query], two 64-query halves;
+                                        // then eight 4 KB dQ staging boxes
   float lse2[2][kBlock];
   float dd[2][kBlock];
   uint64_t bar_kv;
   uint64_t full[2], empty[2];
-  uint64_t s_full, dp_full, ew_done, dvdk_done, dq_full, dq_free, drain;
+  uint64_t s_full, dp_full, ew_done, dvdk_done, dq_full, dq_free, dsbuf_free, drain;
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -74,27 +92,14 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Stages a warp's 32 rows x 32 fp32 columns (lane = row, v = that row's 32
-// values) in 4 KB of shared memory in the layout of a 128-byte-swizzled TMA
-// box (row r's 16-byte chunk c at (c ^ (r & 7)) * 16, conflict-free), then
-// lane 0 adds the box into the dQ accumulator with one bulk tensor
-// reduce-add at (column x, head h, token row).  Before the scratch is
-// rewritten, lane 0 waits for the previous reduce to have read it.
-__device__ __forceinline__ void reduce_rows_tma(uint8_t* scratch, const uint32_t (&v)[32],
-                                                const CUtensorMap* map, int x, int h, int row,
-                                                int lane) {
-  if (lane == 0) bulk_wait_read();
-  __syncwarp();
-  uint8_t* mine = scratch + lane * 128;
+// values) as one 4 KB box in the layout of a 128-byte-swizzled TMA box (row
+// r's 16-byte chunk c at (c ^ (r & 7)) * 16, conflict-free).
+__device__ __forceinline__ void stage_rows32(uint8_t* box, const uint32_t (&v)[32], int lane) {
+  uint8_t* mine = box + lane * 128;
 #pragma unroll
   for (int c = 0; c < 8; ++c)
     *reinterpret_cast<uint4*>(mine + ((c ^ (lane & 7)) << 4)) =
         make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-  fence_proxy_async_smem();   // generic-proxy writes -> visible to the bulk copy
-  __syncwarp();
-  if (lane == 0) {
-    tma_reduce_add_3d(map, scratch, x, h, row);
-    bulk_commit();
-  }
 }
 
 template <int D>
@@ -137,14 +142,15 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.ew_done, 256);
+    mbar_init(&sm.ew_done, 256);        // eight element-wise warps
     mbar_init(&sm.dvdk_done, 1);
     mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_free, 256);
+    mbar_init(&sm.dq_free, 128);        // the dQ warpgroup
+    mbar_init(&sm.dsbuf_free, 128);
     mbar_init(&sm.drain, 1);
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     tmem_alloc(&sm.tmem_slot, 512);
     tmem_relinquish();
   }
@@ -156,9 +162,10 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   constexpr int kHalves = D / 64;
   constexpr uint32_t kDV = 0, kDK = 128, kS = 256, kDP = 384, kDQ = 384;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && nsteps > 0) {
+  if (warp >= kWarpProducer) {
+    warpgroup_regs_dec<kRegsCtl>();
+    if (warp == kWarpProducer && lane == 0 && nsteps > 0) {
+      // ---------------------------------------------------------- producer
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_do);
       mbar_arrive_expect_tx(&sm.bar_kv, 2 * kTileBytes);
@@ -187,10 +194,8 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int n = (issued > 2 ? issued - 2 : 0); n < issued; ++n)
           mbar_drain(&sm.full[n & 1], (n >> 1) & 1);
       }
-    }
-  } else if (warp == 1) {
-    // -------------------------------------------------------- MMA issuer
-    if (lane == 0 && nsteps > 0) {
+    } else if (warp == kWarpMma && lane == 0 && nsteps > 0) {
+      // -------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdescSS = idesc_bf16_f32(kBlock, kBlock, 0, 0);   // K-major both
       constexpr uint32_t kIdescTS = idesc_bf16_f32(kBlock, D, 0, 1);        // B MN-major
       constexpr uint32_t kIdescDQ = idesc_bf16_f32(kBlock, D, 1, 1);        // A, B MN-major
@@ -225,8 +230,8 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         umma_commit(&sm.dp_full);
         if (!(ok = mbar_wait(&sm.ew_done, n & 1, ab))) break;
         tc_fence_after();
-        // dQ first: its read-out and atomics then overlap the dV/dK MMAs,
-        // and the next dP^T (same TMEM columns) is not held up by them.
+        // dQ first: its read-out and adds then overlap the dV/dK MMAs, and
+        // the next dP^T (same TMEM columns) is not held up by them.
 #pragma unroll
         for (int kk = 0; kk < kBlock / 16; ++kk)
           umma_ss(tbase + kDQ, sdesc_sw128(dsbase + kk * 2048, kBlock * 128, 1024),
@@ -254,9 +259,60 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         mbar_drain(&sm.drain, 0);
       }
     }
+  } else if (warp < kWarpEw0) {
+    // --------------------------------------------------------- dQ warpgroup
+    // Warp q reads dQ rows 32q .. 32q+31 (its TMEM lane quarter) in rounds
+    // of 64 columns, stages each round as two 4 KB boxes in slots 2q, 2q+1
+    // of the dS tile and issues their reduce-adds.  TMEM is released as soon
+    // as the last round is in registers; the dS tile once the reduces have
+    // read it.
+    warpgroup_regs_dec<kRegsDq>();
+    const int quarter = warp;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    uint8_t* box0 = reinterpret_cast<uint8_t*>(sm.ds) + (2 * quarter) * 4096;
+    uint8_t* box1 = box0 + 4096;
+    bool ok = true;
+    for (int n = 0; ok && n < nsteps; ++n) {
+      const int32_t h = kvh * g + n % g;
+      const int32_t qa = kb + n / g;
+      const int row0 = qa * kBlock + quarter * 32;
+      if (!(ok = mbar_wait_warp(&sm.dq_full, n & 1, ab))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int rd = 0; rd < D / 64; ++rd) {
+        uint32_t ra[32], rb[32];
+        tmem_ld32x2(tbase + lane_off + kDQ + rd * 64, tbase + lane_off + kDQ + rd * 64 + 32, ra,
+                    rb);
+        if (rd == D / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(&sm.dq_free);       // the dQ columns are in registers
+        }
+        if (rd > 0) {                     // the previous round's reduces must have read the slots
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+        }
+        stage_rows32(box0, ra, lane);
+        stage_rows32(box1, rb, lane);
+        fence_proxy_async_smem();         // generic-proxy writes -> visible to the bulk copy
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tm_dq, box0, rd * 64, h, row0);
+          tma_reduce_add_3d(&tm_dq, box1, rd * 64 + 32, h, row0);
+          bulk_commit();
+        }
+      }
+      if (lane == 0) bulk_wait_read();
+      __syncwarp();
+      mbar_arrive(&sm.dsbuf_free);        // the element-wise warps may rewrite the tile
+    }
+    // The last reduces must have landed before a later kernel reads the
+    // accumulator (and have read the tile before the CTA exits).
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   } else {
     // ------------------------------------------------ element-wise warps
-    const int w = (warp - 2) >> 2;          // query half
+    warpgroup_regs_inc<kRegsEw>();
+    const int w = (warp - kWarpEw0) >> 2;   // query half
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;      // key row (TMEM lane)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -265,7 +321,6 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool ok = true;
     for (int n = 0; ok && n < nsteps; ++n) {
       const int s = n & 1;
-      const int32_t h = kvh * g + n % g;
       const int32_t qa = kb + n / g;
       const bool partial = (qa == kb) || (qa > col_full_hi);
       if (!(ok = mbar_wait_warp(&sm.s_full, n & 1, ab))) break;
@@ -332,10 +387,9 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       tmem_st32(tbase + lane_off + kS + w * 64, pk);
       tmem_st32(tbase + lane_off + kS + w * 64 + 32, dsw);
       // dS^T row r, queries w*64 .. w*64+63 -> swizzled [key][query] half w.
-      // These 4 KB also stage this warp's dQ rows: the previous step's
-      // reduce must have read them first.
-      if (lane == 0) bulk_wait_read();
-      __syncwarp();
+      // The tile staged the previous pair's dQ: the dQ warps release it once
+      // their reduces have read it.
+      if (n > 0 && !(ok = mbar_wait_warp(&sm.dsbuf_free, (n - 1) & 1, ab))) break;
       {
         uint8_t* row = reinterpret_cast<uint8_t*>(sm.ds) + w * (kBlock * 128) + r * 128;
 #pragma unroll
@@ -347,35 +401,7 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.ew_done);
-      // dQ rows (TMEM lane = query row), columns w*D/2 .. of this head.
-      if (!(ok = mbar_wait_warp(&sm.dq_full, n & 1, ab))) break;
-      tc_fence_after();
-      // The warp's dQ rows go out through its own 4 KB of the dS tile (the
-      // dQ MMA that read it has completed; the warp rewrites it only with the
-      // next dS, after the reduce has read it) as bulk tensor reduce-adds.
-      uint8_t* scratch =
-          reinterpret_cast<uint8_t*>(sm.ds) + w * (kBlock * 128) + quarter * 32 * 128;
-      const int row0 = qa * kBlock + quarter * 32;
-      const uint32_t dq_col = tbase + lane_off + kDQ + w * (D / 2);
-      if constexpr (D == 128) {
-        uint32_t ra[32], rb[32];
-        tmem_ld32x2(dq_col, dq_col + 32, ra, rb);
-        tc_fence_before();
-        mbar_arrive(&sm.dq_free);     // TMEM read done; the adds below need only registers
-        reduce_rows_tma(scratch, ra, &tm_dq, w * 64, h, row0, lane);
-        reduce_rows_tma(scratch, rb, &tm_dq, w * 64 + 32, h, row0, lane);
-      } else {
-        uint32_t ra[32];
-        tmem_ld32(dq_col, ra);
-        tc_fence_before();
-        mbar_arrive(&sm.dq_free);
-        reduce_rows_tma(scratch, ra, &tm_dq, w * 32, h, row0, lane);
-      }
     }
-    // The last reduces must have read the scratch before the CTA exits, and
-    // have landed before a later kernel reads the accumulator.
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
     // ---------------------------------------------------------- epilogue
     __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(jkey) * p.Hkv + kvh) * D + w * (D / 2);
     __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(jkey) * p.Hkv + kvh) * D + w * (D / 2);
@@ -411,7 +437,7 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kWarpMma) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tbase, 512);

@@ -63,6 +63,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same with a suspend-time hint: a thread whose phase is not complete sleeps
+// until it completes or `hint_ns` nanoseconds pass, instead of spinning (a
+// spinning warp takes issue slots from the warps that share its scheduler).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kSuspendHintNs = 1000000;   // 1 ms per sleep; the abort flag is polled in between
+
 // Abort state shared by the CTA: set once any wait runs out of time.
 struct AbortState {
   volatile int* cta_flag;   // shared memory
@@ -77,8 +94,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
     if (*ab.cta_flag) return false;
     if (globaltimer_ns() - t0 > ab.limit_ns) {
       *ab.cta_flag = 1;
@@ -158,6 +174,19 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 // Make generic-proxy shared-memory writes visible to the async proxy (MMA/TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Per-thread register budget of the calling warpgroup (all four warps execute
+// it): .dec hands registers back to the CTA's pool, .inc waits until the pool
+// can grant them.  The budgets of all warpgroups must fit in the registers the
+// CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void warpgroup_regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void warpgroup_regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------- tcgen05/TMEM

@@ -25,7 +25,7 @@ cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tdq, const int32_t* key_reach,
                                  const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
                                  int32_t d, float scale, void* dk, void* dv, void* workspace,
-                                 int32_t* status, cudaStream_t s);
+                                 int32_t* status, cudaStream_t s, int num_sms);
 cudaError_t launch_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
                                    void* workspace, void* dq, int32_t* status, cudaStream_t s,
                                    int num_sms);
@@ -242,7 +242,7 @@ tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v, co
     return TREE_ERR_CUDA;
   return cuda_result(tree::launch_attn_bwd_main(tq, tk, tv, tdo, tdq, key_reach, blockmap, T_pad,
                                                 Hq, Hkv, d, scale, dk, dv, workspace, dev_status,
-                                                stream));
+                                                stream, num_sms_current()));
 }
 
 tree_status_t tree_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,

@@ -80,7 +80,7 @@ struct BwdParams {
   float* dq_acc;              // [T_pad, Hq, D]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int32_t T_pad, Hq, Hkv, nb;
+  int32_t T_pad, Hq, Hkv, nb, num_sms;
   float scale, scale_log2;
   int32_t* status;
 };
@@ -119,18 +119,21 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BlockmapView bm{p.nb, const_cast<int32_t*>(p.blockmap)};
-  // CTAs run kv-head-major with key blocks ascending: the CTAs resident at
-  // any moment hold neighbouring key blocks of one kv head, so they stream
-  // the same Q/dO tiles and add into the same dQ rows close together in
-  // time (L2 reuse).  Early key blocks carry the longest columns, so the
-  // order is also roughly heaviest first within each head.
-  const int32_t kvh = blockIdx.x / p.nb;
-  const int32_t kb = blockIdx.x % p.nb;
   const int32_t g = p.Hq / p.Hkv;
-  const int32_t col_hi = bm.col_hi()[kb];
-  const int32_t col_full_hi = bm.col_full_hi()[kb];
-  const int32_t col_len = col_hi >= kb ? col_hi - kb + 1 : 0;
-  const int32_t nsteps = col_len * g;
+  // Launch order.  A column longer than nnz / #SMs tiles would outlast its
+  // kv head's share of the run, so such "heavy" columns are launched first
+  // (for every kv head); they would otherwise start late and form a tail.
+  // Both the heavy and the light CTAs run kv-head-major and heaviest column
+  // first (the blockmap's column order): the CTAs resident at any moment
+  // mostly serve one kv head, so they stream the same Q/dO tiles and add
+  // into the same dQ rows close together in time (L2 reuse).  The light
+  // CTAs take the kv heads in reverse, starting with the one whose heavy
+  // columns ran last.  Each thread tests one or more columns; the counts
+  // are summed by the prologue barrier(s) below.
+  const int32_t heavy_len = bm.base[1] / (p.num_sms > 0 ? p.num_sms : 1);
+  int heavy_local = 0;
+  for (int32_t k = threadIdx.x; k < p.nb; k += kBwdThreads)
+    heavy_local += (bm.col_hi()[k] - k + 1) > heavy_len;
   AbortState ab{&sm.abort_flag, p.status};
 
   if (threadIdx.x == 0) {
@@ -155,9 +158,24 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  int32_t heavy_n = __syncthreads_count(heavy_local > 0);
+  for (int i = 1; i * kBwdThreads < p.nb; ++i) heavy_n += __syncthreads_count(heavy_local > i);
   tc_fence_after();
   const uint32_t tbase = sm.tmem_slot;
+  int32_t kvh, rank;
+  if (static_cast<int32_t>(blockIdx.x) < heavy_n * p.Hkv) {
+    kvh = blockIdx.x / heavy_n;
+    rank = blockIdx.x % heavy_n;
+  } else {
+    const int32_t j = blockIdx.x - heavy_n * p.Hkv, nl = p.nb - heavy_n;
+    kvh = p.Hkv - 1 - j / nl;
+    rank = heavy_n + j % nl;
+  }
+  const int32_t kb = bm.col_order()[rank];
+  const int32_t col_hi = bm.col_hi()[kb];
+  const int32_t col_full_hi = bm.col_full_hi()[kb];
+  const int32_t col_len = col_hi >= kb ? col_hi - kb + 1 : 0;
+  const int32_t nsteps = col_len * g;
   constexpr uint32_t kTileBytes = kBlock * D * 2;
   constexpr int kHalves = D / 64;
   constexpr uint32_t kDV = 0, kDK = 128, kS = 256, kDP = 384, kDQ = 384;
@@ -543,7 +561,7 @@ cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tdq, const int32_t* key_reach,
                                  const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
                                  int32_t d, float scale, void* dk, void* dv, void* workspace,
-                                 int32_t* status, cudaStream_t s) {
+                                 int32_t* status, cudaStream_t s, int num_sms) {
   BwdWorkspace w = carve(workspace, T_pad, Hq, d);
   BwdParams p;
   p.key_reach = key_reach;
@@ -557,6 +575,7 @@ cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.nb = T_pad / kBlock;
+  p.num_sms = num_sms;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;

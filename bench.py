@@ -2,7 +2,11 @@
 
 One step = the whole hot path over one batch of the workload: for every trie
 of the batch, position ids + key reach (a1), blockmap (a2), attention forward
-(a3), backward prepare / main / finish (a4-a6).  Default workload: GRPO-style
+(a3), backward prepare / main / finish (a4-a6).  The tries of a batch are
+independent, so consecutive tries alternate over two CUDA streams (each with
+its own backward workspace): one trie's kernels fill the SMs that another
+trie's kernel tails and small kernels leave idle.  The per-kernel roofline
+figures come from a separate pass that runs the tries on one stream.  Default workload: GRPO-style
 groups (64 prompts x 8 responses, first-fit-decreasing into 32768-token tries,
 Qwen3-8B attention heads 32 q / 8 kv, head_dim 128), seeded synthetic data.
 
@@ -293,8 +297,11 @@ def run_ours(args, rank, ws):
         seqs = [s for i, s in enumerate(seqs) if i in used]
     cases = [TrieCase(ptg, tr, wl, seed, i, device) for i, tr in enumerate(tries)]
     ws_bytes = max(ptg.attn_bwd_workspace_bytes(c.T, wl.Hq, wl.d) for c in cases)
-    ws_bwd = torch.empty((ws_bytes + 3) // 4, dtype=torch.float32, device=device)
-    stream = torch.cuda.Stream(device=device)
+    n_streams = max(1, min(args.streams, len(cases)))
+    ws_bwds = [torch.empty((ws_bytes + 3) // 4, dtype=torch.float32, device=device)
+               for _ in range(n_streams)]
+    streams = [torch.cuda.Stream(device=device) for _ in range(n_streams)]
+    stream = streams[0]
     pairs = sum(c.pairs for c in cases)
     tokens = sum(c.n_tokens for c in cases)
     original = sum(len(s) for s in seqs)
@@ -303,10 +310,26 @@ def run_ours(args, rank, ws):
     bwd_flops = BWD_FLOPS_PER_PAIR * wl.d * wl.Hq * pairs
     fwd_flops = FWD_FLOPS_PER_PAIR * wl.d * wl.Hq * pairs
 
-    def step(ev_list=None):
+    def step():
+        """The whole batch, trie i on stream i % n_streams; joined on streams[0]."""
+        start = torch.cuda.Event()
+        start.record(stream)
+        for st in streams[1:]:
+            st.wait_event(start)
+        for i, c in enumerate(cases):
+            st = streams[i % n_streams]
+            with torch.cuda.stream(st):
+                run_path(ptg, c, ws_bwds[i % n_streams], st)
+        for st in streams[1:]:
+            done = torch.cuda.Event()
+            done.record(st)
+            stream.wait_event(done)
+
+    def serial_step(ev_list):
+        """The whole batch on one stream, with per-kernel events."""
         with torch.cuda.stream(stream):
             for i, c in enumerate(cases):
-                run_path(ptg, c, ws_bwd, stream, None if ev_list is None else ev_list[i])
+                run_path(ptg, c, ws_bwds[0], stream, ev_list[i])
 
     # ---- warm-up (also checks that nothing failed)
     for _ in range(args.warmup):
@@ -324,18 +347,26 @@ def run_ours(args, rank, ws):
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for _ in range(args.steps):
-            evs = [[mk() for _ in range(4)] for _ in cases]
             s0, s1 = mk(), mk()
             s0.record(stream)
-            step(evs)
+            step()
             s1.record(stream)
-            per_step.append((s0, s1, evs))
+            per_step.append((s0, s1))
         torch.cuda.synchronize()
     barrier(ws)
     launches = ptg.launch_count() - launches0
-    fwd_ms = sum(ev[0].elapsed_time(ev[1]) for _, _, evs in per_step for ev in evs)
-    bwd_main_ms = sum(ev[2].elapsed_time(ev[3]) for _, _, evs in per_step for ev in evs)
-    step_ms = [a.elapsed_time(b) for a, b, _ in per_step]
+    step_ms = [a.elapsed_time(b) for a, b in per_step]
+    # per-kernel times: the same batch on one stream, every launch bracketed
+    # by events on the stream it runs on
+    roof_steps = max(1, min(args.steps, 2))
+    serial = []
+    for _ in range(roof_steps):
+        evs = [[mk() for _ in range(4)] for _ in cases]
+        serial_step(evs)
+        serial.append(evs)
+    torch.cuda.synchronize()
+    fwd_ms = sum(ev[0].elapsed_time(ev[1]) for evs in serial for ev in evs) * args.steps / roof_steps
+    bwd_main_ms = sum(ev[2].elapsed_time(ev[3]) for evs in serial for ev in evs) * args.steps / roof_steps
     ms_per_step = float(np.mean(step_ms))
     ms_max = max_over_ranks(ms_per_step, ws)
     flops_all = sum_over_ranks(flops, ws)
@@ -367,7 +398,9 @@ def run_ours(args, rank, ws):
     # ---- end to end through the API with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(ptg, cases, ws_bwd, stream, args, ws, flops_all)
+        # one compute stream here: with the host copies in flight, a second
+        # compute stream measured slower end to end
+        e2e = run_e2e(ptg, cases, ws_bwds[:1], streams[:1], args, ws, flops_all)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
@@ -383,8 +416,9 @@ def run_ours(args, rank, ws):
             "flops_saved_vs_unpacked_causal": round(1 - pairs / causal_pairs, 4),
             "heads": f"{wl.Hq}q/{wl.Hkv}kv", "head_dim": wl.d,
             "packed_tokens_per_s": round(tokens_all / (ms_max * 1e-3), 1),
-            "fwd_ms_per_step": round(fwd_ms / args.steps, 3),
-            "bwd_main_ms_per_step": round(bwd_main_ms / args.steps, 3),
+            "streams": n_streams,
+            "fwd_ms_per_step_one_stream": round(fwd_ms / args.steps, 3),
+            "bwd_main_ms_per_step_one_stream": round(bwd_main_ms / args.steps, 3),
             "l2": "inputs larger than L2 (no flush needed)",
             "parallelism": f"replicas x{ws}",
         },
@@ -402,10 +436,11 @@ def run_ours(args, rank, ws):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(ptg, cases, ws_bwd, stream, args, ws, flops_all):
+def run_e2e(ptg, cases, ws_bwds, streams, args, ws, flops_all):
     """Same metric, each step copying its inputs host->device from pinned
     memory and its outputs (O, dQ, dK, dV) device->host, through the same
-    API calls; copies overlap compute on a second stream."""
+    API calls; copies overlap compute on their own streams.  The tries
+    alternate over the given compute streams."""
     import torch
     # Pinned host copies of every input and output.  Keep them well inside the
     # host's available memory: if the whole batch does not fit in 40% of it,
@@ -436,9 +471,12 @@ def run_e2e(ptg, cases, ws_bwd, stream, args, ws, flops_all):
     copy_in = torch.cuda.Stream()
     copy_out = torch.cuda.Stream()
 
+    n_streams = len(streams)
+
     def e2e_step():
         # outputs of the previous step must be downloaded before they are rewritten
-        stream.wait_stream(copy_out)
+        for st in streams:
+            st.wait_stream(copy_out)
         ready = []
         for i, c in enumerate(cases):
             with torch.cuda.stream(copy_in):
@@ -449,18 +487,20 @@ def run_e2e(ptg, cases, ws_bwd, stream, args, ws, flops_all):
             ready.append(ev)
         done = []
         for i, c in enumerate(cases):
-            stream.wait_event(ready[i])
-            with torch.cuda.stream(stream):
-                run_path(ptg, c, ws_bwd, stream)
+            st = streams[i % n_streams]
+            st.wait_event(ready[i])
+            with torch.cuda.stream(st):
+                run_path(ptg, c, ws_bwds[i % n_streams], st)
                 ev = torch.cuda.Event()
-                ev.record(stream)
+                ev.record(st)
             done.append(ev)
             copy_out.wait_event(ev)
             with torch.cuda.stream(copy_out):
                 for dst, src in zip(host_out[i], c.output_tensors()):
                     dst.copy_(src, non_blocking=True)
         # the next step's uploads must not overwrite inputs still in use
-        copy_in.wait_stream(stream)
+        for st in streams:
+            copy_in.wait_stream(st)
 
     for _ in range(max(1, min(args.warmup, 2))):
         e2e_step()
@@ -503,6 +543,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--tries", type=int, default=0,
                     help="use only the first N tries of the batch (small profiling cases)")
+    ap.add_argument("--streams", type=int, default=2,
+                    help="CUDA streams the independent tries of a batch alternate over")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0,

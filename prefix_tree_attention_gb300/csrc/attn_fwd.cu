@@ -18,10 +18,12 @@
 //              need no shuffles.  P is written back as bf16 over the first
 //              64 columns of S_t and consumed there by the PV MMA.
 // TMEM: S_0 [0,128) S_1 [128,256) O_0 [256,256+d) O_1 [384,384+d).
-// The issuer starts QK of tile k+1 for a head slot only after PV of tile k
-// for that slot has completed, so P/S aliasing is safe and the O rescale in
-// the softmax warps never races an MMA; the two slots interleave on the
-// tensor pipe.  The running max is refreshed only when it grows by more than
+// tcgen05.mma operations issued by one thread execute in issue order, so the
+// issuer queues QK of tile k+1 for a head slot right behind PV of tile k
+// (PV reads P from the S columns before the later QK writes them) instead of
+// draining the pipe to wait for PV to finish; the softmax of tile k+1 starts
+// only once QK(k+1) has completed, so PV(k) is done by then and its O
+// rescale never races an MMA.  The two slots interleave on the tensor pipe.  The running max is refreshed only when it grows by more than
 // 8 (log2 units): P stays <= 256, and O is rescaled in TMEM only then.
 #include <cuda_bf16.h>
 
@@ -381,9 +383,7 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (!(ok = mbar_wait(&sm.kv_full[s1], ((k + 1) >> 1) & 1, ab))) break;
             next_loaded = true;
           }
-          if (!(ok = mbar_wait(&sm.o_full[t], k & 1, ab))) break;   // P_t(k) consumed
-          tc_fence_after();
-          issue_qk(t, smem_u32(sm.k[s1]));
+          issue_qk(t, smem_u32(sm.k[s1]));       // in order behind PV_t(k)
         }
       }
       if (!ok) {

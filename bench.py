@@ -336,6 +336,9 @@ def run_ours(args, rank, ws):
         step()
     torch.cuda.synchronize()
     bad = [int(c.bufs.status.item()) for c in cases if int(c.bufs.status.item()) != 0]
+    # non-empty 128x128 tiles of every trie (blockmap word 1), read once here:
+    # bwd main adds one 128 x d fp32 dQ tile per (non-empty tile, query head)
+    nnz_tiles = sum(int(c.bufs.blockmap[1].item()) for c in cases)
     if bad:
         raise RuntimeError(f"device status {ptg.status_string(bad[0])} during warm-up")
 
@@ -380,6 +383,7 @@ def run_ours(args, rank, ws):
     peaks = measured_peaks()
     n_launch = len(cases) * args.steps
     bwd_achieved = bwd_flops * args.steps / (bwd_main_ms * 1e-3) / 1e12
+    dq_bytes = float(nnz_tiles) * wl.Hq * 128 * wl.d * 4
     fwd_achieved = fwd_flops * args.steps / (fwd_ms * 1e-3) / 1e12
     traffic = recorded_traffic()
     roofline = {
@@ -393,6 +397,13 @@ def run_ours(args, rank, ws):
         "flops_per_launch": bwd_flops / len(cases),
         "fwd_achieved": round(fwd_achieved, 1),
         "fwd_frac": round(fwd_achieved / peaks["bf16_sustained"], 4),
+        # the dQ accumulation: fp32 reduce-adds at L2, the step's other limit
+        "dq_reduce": {
+            "bytes_per_launch": dq_bytes / len(cases),
+            "achieved_GBps": round(dq_bytes * args.steps / (bwd_main_ms * 1e-3) / 1e9, 1),
+            "note": "bulk tensor reduce-adds of 32x32 fp32 boxes; a stand-alone "
+                    "measurement on GB300 tops out at 4000-4400 GB/s",
+        },
     }
 
     # ---- end to end through the API with host buffers

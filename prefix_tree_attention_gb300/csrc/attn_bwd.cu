@@ -224,10 +224,10 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (!(ok = mbar_wait(&sm.full[s], (n >> 1) & 1, ab))) break;
         tc_fence_after();
         const uint32_t qbase = smem_u32(sm.q[s]), obase = smem_u32(sm.dout[s]);
-        if (n > 0) {
-          if (!(ok = mbar_wait(&sm.dvdk_done, (n - 1) & 1, ab))) break;
-          tc_fence_after();
-        }
+        // S^T(n) overwrites the columns that held P^T(n-1) and dS^T(n-1).  It
+        // is queued behind dV(n-1) and dK(n-1), and tcgen05.mma operations of
+        // one thread execute in issue order, so those reads come first and the
+        // pipe is not drained here.
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (kBlock * 128) + (kk & 3) * 32;

@@ -15,8 +15,13 @@ visible pairs count only unmasked (i, j) over real tokens (4 d Hq per pair
 for the forward, 10 d Hq for the backward).  Packed tokens/s is reported too.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-Under torchrun each rank runs its own batch (seed = rank): weak scaling, no
-collective on the data path; rank 0 prints one JSON line.
+                       [--split replicas|balanced]
+Under torchrun each rank runs its own batch (seed = rank, --split replicas,
+the default): weak scaling, no collective on the data path.  With --split
+balanced every rank takes the same global batch and keeps one group of the
+library's load-balanced partition (contiguous segments of the batch's DFS
+order, largest per-rank prefix-tree token count minimised): strong scaling.
+Rank 0 prints one JSON line.
 """
 from __future__ import annotations
 
@@ -45,6 +50,19 @@ KERNEL_SOURCE = os.path.join(ROOT, "prefix_tree_attention_gb300", "csrc", "attn_
 
 
 # ------------------------------------------------------------------ helpers
+def rank_batch(ptg, key: str, seed: int, rank: int, world: int, split: str):
+    """Sequences this rank trains on, and the seed of its tensor data.
+
+    replicas: an independent batch per rank (seed + rank).
+    balanced: the global batch (seed) split over the ranks by the library's
+    load-balanced partitioner; rank r keeps group r."""
+    if split == "replicas" or world == 1:
+        return W.sequences(key, seed + rank), seed + rank
+    seqs = W.sequences(key, seed)
+    groups, _cost, _mx = ptg.partition_sequences(seqs, world)
+    return [sq for sq, g in zip(seqs, groups.tolist()) if g == rank], seed + rank
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -288,8 +306,7 @@ def run_ours(args, rank, ws):
     torch.cuda.set_device(local)
     device = f"cuda:{local}"
     wl = W.WORKLOADS[args.workload]
-    seed = args.seed + rank
-    seqs = W.sequences(args.workload, seed)
+    seqs, seed = rank_batch(ptg, args.workload, args.seed, rank, ws, args.split)
     tries = ptg.pack_sequences(seqs, wl.max_tokens_per_mb)
     if args.tries:
         tries = tries[:args.tries]
@@ -416,8 +433,9 @@ def run_ours(args, rank, ws):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
+        "higher_is_better": True,
+        "scaling": "strong" if (args.split == "balanced" and ws > 1) else "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {
             "workload": args.workload + (f" (first {args.tries} tries)" if args.tries else ""),
             "description": wl.description,
@@ -431,7 +449,8 @@ def run_ours(args, rank, ws):
             "fwd_ms_per_step_one_stream": round(fwd_ms / args.steps, 3),
             "bwd_main_ms_per_step_one_stream": round(bwd_main_ms / args.steps, 3),
             "l2": "inputs larger than L2 (no flush needed)",
-            "parallelism": f"replicas x{ws}",
+            "parallelism": (f"balanced split of one batch x{ws}" if args.split == "balanced"
+                            else f"replicas x{ws}"),
         },
         "roofline": roofline,
         "gpu_launches": launches,
@@ -554,6 +573,9 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--tries", type=int, default=0,
                     help="use only the first N tries of the batch (small profiling cases)")
+    ap.add_argument("--split", choices=["replicas", "balanced"], default="replicas",
+                    help="N > 1: independent batch per rank, or one batch split by the "
+                         "load-balanced partitioner")
     ap.add_argument("--streams", type=int, default=2,
                     help="CUDA streams the independent tries of a batch alternate over")
     ap.add_argument("--no-e2e", action="store_true")

@@ -306,6 +306,37 @@ TREE_API tree_status_t tree_packing_seq_indices(const tree_packing_t* packing, i
                                        int32_t* out, int32_t capacity);
 
 /* ------------------------------------------------------------------------
+ * tree_partition_sequences — load-balanced split of a batch over K workers.
+ *
+ * Source: AREAL-DTA, section 4 (load-balanced parallelisation: problem
+ * formalisation, partition algorithm, binary-search solution).  Each worker
+ * builds one prefix tree from its group; a group's cost is that tree's token
+ * count (the sum of its nodes' token lengths).  The sequences are ordered as
+ * a DFS of the single prefix tree they would form together (lexicographic
+ * order of the token sequences, ties in input order) and cut into at most
+ * n_groups contiguous segments whose largest cost is the smallest possible
+ * for that order: binary search over the bound tau from the longest sequence
+ * to the whole tree's token count, each tau checked by a greedy scan that
+ * starts a new segment when the next sequence would push the current one
+ * past tau.  Segments are numbered in DFS order; when fewer than n_groups
+ * segments are needed, the last groups are empty (cost 0).
+ *
+ *   tokens        [in]  host int32, the sequences concatenated
+ *   seq_offsets   [in]  host int64[n_seqs + 1], sequence s = tokens[off[s], off[s+1])
+ *   n_seqs        number of sequences (>= 1)
+ *   n_groups      number of workers K (>= 1)
+ *   group_of_seq  [out] host int32[n_seqs], the group of every input sequence
+ *   group_cost    [out] host int64[n_groups], token count of each group's tree (may be NULL)
+ *   max_cost      [out] host int64, the largest group cost (may be NULL)
+ * Errors: TREE_ERR_INVALID_ARG for a null required pointer, n_seqs < 1,
+ * n_groups < 1 or an empty sequence.  Pure host code; no device work.
+ * ---------------------------------------------------------------------- */
+TREE_API tree_status_t tree_partition_sequences(const int32_t* tokens, const int64_t* seq_offsets,
+                                                int32_t n_seqs, int32_t n_groups,
+                                                int32_t* group_of_seq, int64_t* group_cost,
+                                                int64_t* max_cost);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  *
  * tree_debug_wait_timeout — launch one warp that waits on a shared-memory

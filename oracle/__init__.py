@@ -19,7 +19,8 @@ Sources (web pages; cited by title and section):
 * "AREAL-DTA: Dynamic Tree Attention for Efficient Reinforcement Learning of
   Large Language Models", section 3 "Problem formalisation" (total loss is the
   sum of per-sequence losses; a shared prefix is computed once and its
-  gradient sums the contributions of every descendant sequence).
+  gradient sums the contributions of every descendant sequence) and section 4
+  "负载均衡并行化" (load-balanced split of a batch over training workers).
 
 Modules:
 
@@ -28,6 +29,8 @@ Modules:
 * ``oracle.mask``      — dense ancestor mask by parent-pointer walks,
                          position ids, 128x128 tile classes.
 * ``oracle.attention`` — masked softmax attention forward/backward in fp64.
+* ``oracle.partition`` — prefix-tree token cost and the optimal contiguous
+                         split of the DFS order over K workers.
 
 Every floating-point routine accumulates in float64 on inputs that were
 already rounded to bf16 by the caller.  Parity status of each function is

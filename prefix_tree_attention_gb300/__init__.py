@@ -55,6 +55,7 @@ _sig = {
     "tree_attn_bwd_finish": (ctypes.c_int, [_I32, _I32, _I32, _F32, _P, _SZ, _P, _P, _P]),
     "tree_launch_count": (ctypes.c_uint64, []),
     "tree_pack_positions_noalloc": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P, _P, _P]),
+    "tree_partition_sequences": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -288,6 +289,31 @@ def pack_sequences(seqs, max_tokens_per_mb: int, block: int = BLOCK, pad_to_max:
         return out
     finally:
         _lib.tree_packing_free(handle)
+
+
+def _flatten(seqs):
+    lens = np.array([len(s) for s in seqs], dtype=np.int64)
+    offs = np.zeros(len(seqs) + 1, dtype=np.int64)
+    np.cumsum(lens, out=offs[1:])
+    flat = np.zeros(max(1, int(offs[-1])), dtype=np.int32)
+    for i, s in enumerate(seqs):
+        flat[offs[i]:offs[i + 1]] = s
+    return flat, offs
+
+
+def partition_sequences(seqs, n_groups: int):
+    """Split token sequences over ``n_groups`` workers with the library's
+    load-balanced partitioner (contiguous segments of the sequences' DFS
+    order, largest per-group prefix-tree token count minimised).  Returns
+    ``(group_of_seq int32[n], group_cost int64[n_groups], max_cost)``."""
+    flat, offs = _flatten(seqs)
+    groups = np.empty(len(seqs), np.int32)
+    cost = np.empty(max(1, int(n_groups)), np.int64)
+    mx = ctypes.c_int64()
+    _check("tree_partition_sequences", _lib.tree_partition_sequences(
+        flat.ctypes.data, offs.ctypes.data, len(seqs), int(n_groups), groups.ctypes.data,
+        cost.ctypes.data, ctypes.byref(mx)))
+    return groups, cost[:int(n_groups)], int(mx.value)
 
 
 # --------------------------------------------------------------- convenience

@@ -76,3 +76,39 @@ def test_recorded_traffic_is_null_when_source_changed(tmp_path, monkeypatch):
     rec["kernel_source_sha256_16"] = bench.source_hash(bench.KERNEL_SOURCE)
     p.write_text(json.dumps(rec))
     assert bench.recorded_traffic() == 123
+
+
+def _split_worker(rank, port, out):
+    import prefix_tree_attention_gb300 as ptg
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE="2")
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    seqs, _seed = bench.rank_batch(ptg, "agent", 0, rank, 2, "balanced")
+    mine = [tuple(x) for x in seqs]
+    gathered = [None, None]
+    dist.all_gather_object(gathered, mine)
+    out[rank] = gathered
+    dist.destroy_process_group()
+
+
+def test_balanced_split_world_size_two_covers_the_batch_once():
+    import workloads as W
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_split_worker, args=(port, out), nprocs=2, start_method="spawn",
+                       join=True)
+    a, b = out[0]
+    assert out[1] == [a, b]
+    batch = [tuple(x) for x in W.sequences("agent", 0)]
+    assert sorted(a + b) == sorted(batch) and a and b
+    # contiguous halves of the DFS (lexicographic) order
+    assert max(a) < min(b)
+
+
+def test_replicas_split_gives_each_rank_its_own_batch():
+    import prefix_tree_attention_gb300 as ptg
+    import workloads as W
+    s0, seed0 = bench.rank_batch(ptg, "tiny", 0, 0, 2, "replicas")
+    s1, seed1 = bench.rank_batch(ptg, "tiny", 0, 1, 2, "replicas")
+    assert s0 == W.sequences("tiny", 0) and s1 == W.sequences("tiny", 1) and seed1 == seed0 + 1

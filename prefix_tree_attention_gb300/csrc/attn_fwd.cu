@@ -271,11 +271,16 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const BlockmapView bm{p.nb, const_cast<int32_t*>(p.blockmap)};
-  // Head-group-major order: the CTAs resident at any moment share one head
-  // group (so one kv head's K/V stays hot in L2) and take query blocks
-  // heaviest row first.
-  const int32_t qa = bm.row_order()[blockIdx.x % p.nb];
-  const int32_t h0 = (blockIdx.x / p.nb) * p.heads_per_cta;
+  // KV-head-major order: the CTAs resident at any moment serve one kv head,
+  // so its K/V tiles stay hot in L2.  Within a kv head, the rows of all its
+  // head groups (which read the same K/V tiles) run together, heaviest row
+  // first, so the last kv head's long rows start with twice the span of a
+  // single head group ahead of them.
+  const int32_t gpk = p.n_hgroups / p.Hkv;          // head groups per kv head
+  const int32_t unit = blockIdx.x / (gpk * p.nb);
+  const int32_t j = blockIdx.x % (gpk * p.nb);
+  const int32_t qa = bm.row_order()[j / gpk];
+  const int32_t h0 = (unit * gpk + j % gpk) * p.heads_per_cta;
   const int nh = p.heads_per_cta;
   const int32_t kvh = h0 / (p.Hq / p.Hkv);
   const int32_t ntiles = bm.row_cnt()[qa];

@@ -14,8 +14,10 @@ Sources (web pages; cited by title and section):
   "核心数据结构：TrieNode" (node spans, preorder ``nodes`` list, virtual root),
   "打包数据的生成" (position ids from the dense mask), the packing figure
   (ancestor mask, worked example [A,B,C,D]/[A,B,E,F]/[A,G,H]),
-  "FlexAttention + BlockMask" (128-token blocks) and
-  "参数背后的源码校验逻辑" (packing validation).
+  "FlexAttention + BlockMask" (128-token blocks),
+  "参数背后的源码校验逻辑" (packing validation) and
+  "Log Probability 计算：树结构的特殊处理" (per-sequence log-probabilities
+  and entropies gathered from packed logits).
 * "AREAL-DTA: Dynamic Tree Attention for Efficient Reinforcement Learning of
   Large Language Models", section 3 "Problem formalisation" (total loss is the
   sum of per-sequence losses; a shared prefix is computed once and its
@@ -31,6 +33,9 @@ Modules:
 * ``oracle.attention`` — masked softmax attention forward/backward in fp64.
 * ``oracle.partition`` — prefix-tree token cost and the optimal contiguous
                          split of the DFS order over K workers.
+* ``oracle.logprob``   — node-internal and transition log-probabilities,
+                         entropies and vocabulary min/max of packed logits,
+                         and the per-sequence merge.
 
 Every floating-point routine accumulates in float64 on inputs that were
 already rounded to bf16 by the caller.  Parity status of each function is

@@ -1,0 +1,189 @@
+"""Oracle tree-aware log-probability / entropy gather — TEST INFRASTRUCTURE ONLY.
+
+Follows the AReaL Tree Training guide, section "Log Probability 计算：树结构的
+特殊处理" (log-probabilities of packed trees), in its order:
+
+1. every sequence of the trie is visited (``trie.all_sequence_ids``);
+2. for every node on the sequence's path two kinds of log-probability are
+   taken:
+   * node-internal: the logits at packed rows ``start .. end-1`` of the node
+     predict its own tokens at rows ``start+1 .. end``;
+   * transition: the logits at the node's last row (``pred_pos = end``)
+     predict the first token of the next node on the path
+     (``label_pos = next_start``);
+3. both are cached, internal pieces by ``(start, end)`` and transitions by
+   ``(pred_pos, label_pos)``, so sequences that share a prefix reuse them;
+4. the pieces are concatenated in path order into the sequence's own
+   log-probability vector.
+
+The same section names the companions: the entropy of the predictive
+distributions (``gather_packed_tree_logprobs_entropy``), vocabulary min/max
+statistics (``gather_packed_tree_vocab_stats``) and the merge of per-sequence
+results of several micro-batches back into a ``[batch, max_len]`` layout
+padded with ``padding_value`` (``merge_packed_tree_results``).
+
+Readings where the page is silent (each stated again in the design doc):
+* the input is the packed logits ``[T_pad, V]`` (one row per packed token);
+  log-softmax is the plain definition ``x - logsumexp(x)`` in float64 on the
+  given values, with no temperature;
+* a sequence of length L has L-1 log-probabilities: entry t is the
+  log-probability of its token t+1 given the logits at the row of its token
+  t.  Its entropy and vocabulary statistics are taken at the same L-1
+  predicting rows (entry t: the distribution of the row of token t);
+* ``chunk_size`` only bounds the page's peak memory and changes no value,
+  so the oracle has no chunking.
+
+Parity: pinned by the worked example of the packing figure (predecessor of
+every token), by the unpack invariant (the tree gather equals the textbook
+per-sequence computation with labels shifted by one, using scipy's
+log_softmax), by closed forms (uniform logits; one dominant logit), by brute
+force over small tries (the predecessor from parent pointers is the last
+visible key before the token in the dense ancestor mask), and by the cache
+count (every non-root-start token is a label exactly once).  See
+tests/test_oracle_logprob.py.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def log_softmax(row) -> np.ndarray:
+    """``x - logsumexp(x)`` in float64, max-shifted."""
+    x = np.asarray(row, dtype=np.float64)
+    m = x.max()
+    return x - (m + np.log(np.exp(x - m).sum()))
+
+
+def row_stats(row):
+    """(logsumexp, entropy, min, max) of one logits row, float64."""
+    x = np.asarray(row, dtype=np.float64)
+    m = x.max()
+    lse = m + np.log(np.exp(x - m).sum())
+    lp = x - lse
+    ent = -(np.exp(lp) * lp).sum()
+    return float(lse), float(ent), float(x.min()), float(m)
+
+
+def path_nodes(packed, sid: int) -> list[int]:
+    """Nodes that sequence ``sid`` passes, root side first."""
+    idx = packed.seq_index[sid]
+    nodes = packed.token_node[idx]
+    out = [int(nodes[0])]
+    for n in nodes[1:]:
+        if int(n) != out[-1]:
+            out.append(int(n))
+    return out
+
+
+class _Gather:
+    """Steps 1-4 over one packed trie, with the page's two caches."""
+
+    def __init__(self, logits, packed):
+        self.logits = logits
+        self.packed = packed
+        self.internal_cache: dict[tuple[int, int], np.ndarray] = {}
+        self.transition_cache: dict[tuple[int, int], float] = {}
+        self.row_cache: dict[int, tuple] = {}
+
+    def _row(self, p: int):
+        if p not in self.row_cache:
+            self.row_cache[p] = (log_softmax(self.logits[p]), row_stats(self.logits[p]))
+        return self.row_cache[p]
+
+    def internal(self, start: int, end: int) -> np.ndarray:
+        key = (start, end)
+        if key not in self.internal_cache:
+            tok = self.packed.token_ids
+            self.internal_cache[key] = np.array(
+                [self._row(p)[0][tok[p + 1]] for p in range(start, end)], dtype=np.float64)
+        return self.internal_cache[key]
+
+    def transition(self, pred_pos: int, label_pos: int) -> float:
+        key = (pred_pos, label_pos)
+        if key not in self.transition_cache:
+            self.transition_cache[key] = float(
+                self._row(pred_pos)[0][self.packed.token_ids[label_pos]])
+        return self.transition_cache[key]
+
+    def sequence(self, sid: int):
+        """(logprob[L-1], entropy[L-1], vocab_min[L-1], vocab_max[L-1])."""
+        pk = self.packed
+        nodes = path_nodes(pk, sid)
+        lps: list[np.ndarray] = []
+        pred_rows: list[int] = []
+        for a, n in enumerate(nodes):
+            start, end = int(pk.node_start[n]), int(pk.node_end[n])
+            lps.append(self.internal(start, end))
+            pred_rows.extend(range(start, end))
+            if a + 1 < len(nodes):
+                nxt = int(pk.node_start[nodes[a + 1]])
+                lps.append(np.array([self.transition(end, nxt)]))
+                pred_rows.append(end)
+        lp = np.concatenate(lps) if lps else np.zeros(0)
+        stats = [self._row(p)[1] for p in pred_rows]
+        ent = np.array([s[1] for s in stats], dtype=np.float64)
+        vmin = np.array([s[2] for s in stats], dtype=np.float64)
+        vmax = np.array([s[3] for s in stats], dtype=np.float64)
+        return lp, ent, vmin, vmax
+
+
+def gather_packed_tree_logprobs_entropy(logits, packed, with_stats: bool = False):
+    """Per-sequence log-probabilities and entropies of one packed trie.
+
+    Returns ``{sid: (logprob, entropy)}`` (or ``(logprob, entropy, vmin, vmax)``
+    with ``with_stats``) and the gather object, whose caches hold every
+    distinct internal and transition piece that was computed.
+    """
+    g = _Gather(logits, packed)
+    out = {}
+    for sid in packed.seq_ids:
+        lp, ent, vmin, vmax = g.sequence(sid)
+        out[sid] = (lp, ent, vmin, vmax) if with_stats else (lp, ent)
+    return out, g
+
+
+def merge_packed_tree_results(results, n_seqs: int, padding_value: float = 0.0,
+                              max_len: int | None = None) -> np.ndarray:
+    """Per-sequence vectors of several micro-batches (a list of
+    ``{sid: vector}``) into ``[n_seqs, max_len]`` by sequence id, short rows
+    padded with ``padding_value``."""
+    merged: dict[int, np.ndarray] = {}
+    for res in results:
+        for sid, vec in res.items():
+            merged[sid] = np.asarray(vec, dtype=np.float64)
+    if max_len is None:
+        max_len = max((v.size for v in merged.values()), default=0)
+    out = np.full((n_seqs, max_len), padding_value, dtype=np.float64)
+    for sid, vec in merged.items():
+        n = min(vec.size, max_len)
+        out[sid, :n] = vec[:n]
+    return out
+
+
+def token_pred(packed) -> np.ndarray:
+    """Packed row whose logits predict each token: the previous token of the
+    same node, else the last token of the parent node; -1 for the first token
+    of a top-level node and for pads.  Walks parent pointers."""
+    pred = np.full(packed.T_pad, -1, np.int32)
+    for j in range(packed.T_pad):
+        n = int(packed.token_node[j])
+        if n < 0:
+            continue
+        if j > int(packed.node_start[n]):
+            pred[j] = j - 1
+        else:
+            par = int(packed.node_parent[n])
+            if par >= 0:
+                pred[j] = int(packed.node_end[par])
+    return pred
+
+
+def packed_token_logprobs(logits, packed) -> np.ndarray:
+    """Per packed token j: log-probability of its token under the logits of
+    its predecessor row (0 where there is none), float64."""
+    pred = token_pred(packed)
+    out = np.zeros(packed.T_pad, np.float64)
+    for j in range(packed.T_pad):
+        if pred[j] >= 0:
+            out[j] = log_softmax(logits[pred[j]])[packed.token_ids[j]]
+    return out

@@ -186,3 +186,18 @@ def tensors(T: int, Hq: int, Hkv: int, d: int, seed: int, stream: int = 0,
     for name, shape in (("q", shape_q), ("k", shape_kv), ("v", shape_kv), ("do", shape_q)):
         out[name] = torch.randn(shape, generator=g, device=device, dtype=torch.bfloat16)
     return out
+
+
+def logits(T: int, V: int, seed: int, device="cpu", dtype=None, sigma: float = 2.0,
+           row_stride: int | None = None):
+    """Packed next-token logits [T, V] drawn as sigma * N(0, 1), rounded to
+    ``dtype`` (bf16 by default).  With ``row_stride`` > V the rows sit in a
+    wider buffer and the view [:, :V] is returned."""
+    import torch
+    dtype = torch.bfloat16 if dtype is None else dtype
+    g = torch.Generator(device=device)
+    g.manual_seed((0x10C1 + 1000033 * seed) & ((1 << 63) - 1))
+    width = V if row_stride is None else row_stride
+    buf = torch.randn((T, width), generator=g, device=device, dtype=torch.float32)
+    buf = (buf * sigma).to(dtype)
+    return buf[:, :V]

@@ -15,7 +15,9 @@ visible pairs count only unmasked (i, j) over real tokens (4 d Hq per pair
 for the forward, 10 d Hq for the backward).  Packed tokens/s is reported too.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--split replicas|balanced]
+                       [--split replicas|balanced] [--path attention|logprob]
+--path logprob times the tree-aware log-probability / entropy gather over the
+same batch instead (bf16 logits over the Qwen3 vocabulary; its own JSON line).
 Under torchrun each rank runs its own batch (seed = rank, --split replicas,
 the default): weak scaling, no collective on the data path.  With --split
 balanced every rank takes the same global batch and keeps one group of the
@@ -466,6 +468,157 @@ def run_ours(args, rank, ws):
         print(json.dumps(line), flush=True)
 
 
+LOGPROB_METRIC = "tree log-prob/entropy gather of packed logits, packed tokens/s"
+QWEN3_VOCAB = 151936
+
+
+def run_logprob(args, rank, ws):
+    """``--path logprob``: the tree-aware log-probability gather over one batch.
+
+    One step = for every trie of the batch, tree_logprobs_entropy over that
+    trie's rows of a bf16 logits buffer [T_pad, 151936] (row log-sum-exp and
+    entropy, then each token's label log-probability), followed by the merge
+    of log-probabilities and entropies into [n_seqs, max_len].  Positions and
+    blockmap (a1, a2) are inputs here.  One 10 GB logits buffer, larger than
+    L2, serves every trie (an LM head would write each micro-batch's logits
+    into such a buffer).  The roofline is the row kernel against HBM: it must
+    read the T_real x V logits once.
+    """
+    import torch
+    import prefix_tree_attention_gb300 as ptg
+    from oracle import logprob as OL
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    wl = W.WORKLOADS[args.workload]
+    seqs, seed = rank_batch(ptg, args.workload, args.seed, rank, ws, args.split)
+    tries = ptg.pack_sequences(seqs, wl.max_tokens_per_mb)
+    if args.tries:
+        tries = tries[:args.tries]
+    used = sorted({s for tr in tries for s in tr.seq_ids})
+    remap = {s: i for i, s in enumerate(used)}
+    for tr in tries:
+        tr.seq_index = {remap[s]: v for s, v in tr.seq_index.items()}
+    V = QWEN3_VOCAB
+    t_max = max(tr.T_pad for tr in tries)
+    logits = W.logits(t_max, V, seed=seed, device=device)
+    offs = np.cumsum([0] + [tr.T_pad for tr in tries]).tolist()
+    total = offs[-1]
+    f32 = dict(dtype=torch.float32, device=device)
+    lse_all, ent_all, lp_all = (torch.empty(total, **f32) for _ in range(3))
+    cases = []
+    for tr in tries:
+        bufs = ptg.TrieBuffers(tr.T_pad, tr.n_nodes, 1, 64, device=device)
+        tn = torch.from_numpy(tr.token_node).to(device)
+        ptg.tree_pack_positions(tn, torch.from_numpy(tr.node_entry).to(device),
+                                torch.from_numpy(tr.node_exit).to(device), bufs.position_ids,
+                                bufs.key_reach, bufs.pos_ws, bufs.status)
+        ptg.tree_blockmap_build(bufs.key_reach, bufs.blockmap, bufs.status)
+        # the workload's fresh token ids run past the vocabulary: fold them in
+        tok = np.where(tr.token_ids >= 0, tr.token_ids % V, -1).astype(np.int32)
+        cases.append((tr, bufs, torch.from_numpy(tok).to(device)))
+    pos, soffs = ptg.sequence_index_arrays(tries, len(used), offs[:-1])
+    pos_d = torch.from_numpy(pos).to(device)
+    soffs_d = torch.from_numpy(soffs).to(device)
+    max_len = max(int(soffs[i + 1] - soffs[i]) for i in range(len(used))) - 1
+    out_lp = torch.empty((len(used), max_len), **f32)
+    out_ent = torch.empty_like(out_lp)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+    tokens = sum(tr.n_tokens for tr in tries)
+
+    def step():
+        for i, (tr, bufs, tok) in enumerate(cases):
+            sl = slice(offs[i], offs[i + 1])
+            ptg.tree_logprobs_entropy(logits[:tr.T_pad], bufs.key_reach, lse_all[sl],
+                                      bufs.status, token_ids=tok, blockmap=bufs.blockmap,
+                                      entropy=ent_all[sl], logprob=lp_all[sl])
+        ptg.tree_merge_per_sequence(lp_all, pos_d, soffs_d, out_lp, status, 1, 1, 0.0)
+        ptg.tree_merge_per_sequence(ent_all, pos_d, soffs_d, out_ent, status, 0, 1, 0.0)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bad = [int(b.status.item()) for _, b, _ in cases] + [int(status.item())]
+    if any(bad):
+        raise RuntimeError("device status " + ptg.status_string(max(bad)))
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    launches0 = ptg.launch_count()
+    barrier(ws)
+    torch.cuda.synchronize()
+    per_step = []
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            s0, s1 = mk(), mk()
+            s0.record(stream)
+            step()
+            s1.record(stream)
+            per_step.append((s0, s1))
+        torch.cuda.synchronize()
+    barrier(ws)
+    launches = ptg.launch_count() - launches0
+    ms_per_step = float(np.mean([a.elapsed_time(b) for a, b in per_step]))
+    ms_max = max_over_ranks(ms_per_step, ws)
+    tokens_all = sum_over_ranks(tokens, ws)
+    # the row kernel alone (no label pass): each launch bracketed by events
+    row_ms = 0.0
+    for tr, bufs, tok in cases:
+        e0, e1 = mk(), mk()
+        e0.record(stream)
+        ptg.tree_logprobs_entropy(logits[:tr.T_pad], bufs.key_reach, lse_all[:tr.T_pad],
+                                  bufs.status, entropy=ent_all[:tr.T_pad])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        row_ms += e0.elapsed_time(e1)
+    row_bytes = sum(tr.n_tokens * (V * 2 + 8) + tr.T_pad * 4 for tr in tries)
+    peaks = measured_peaks()
+    achieved = row_bytes / (row_ms * 1e-3) / 1e9
+    line = {
+        "metric": LOGPROB_METRIC, "value": round(tokens_all / (ms_max * 1e-3), 1),
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 3), "higher_is_better": True,
+        "scaling": "strong" if (args.split == "balanced" and ws > 1) else "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": args.workload + (f" (first {args.tries} tries)" if args.tries else ""),
+            "path": "logprob", "tries": len(tries), "packed_tokens": tokens,
+            "sequences": len(used), "vocab": V, "logits": "bf16 sigma*N(0,1), sigma 2",
+            "logits_gb_read_per_step": round(row_bytes / 1e9, 2),
+            "l2": "logits larger than L2 (no flush needed)",
+            "parallelism": (f"balanced split of one batch x{ws}" if args.split == "balanced"
+                            else f"replicas x{ws}"),
+        },
+        "roofline": {
+            "kernel": "k_row_stats (row log-sum-exp / entropy)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": peaks["hbm"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm"], 4),
+            "peak_kind": f"HBM copy ({peaks['source']})", "traffic": None,
+            "avg_launch_ms": round(row_ms / len(cases), 4),
+            "bytes_per_launch": row_bytes / len(cases),
+        },
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": None,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle's row reduction and label gather on host rows of the same logits
+        rows = min(64, tries[0].n_tokens)
+        host = logits[:rows].float().cpu().numpy().astype(np.float64)
+        t0 = time.perf_counter()
+        done = 0
+        while time.perf_counter() - t0 < min(args.cpu_budget, 10.0):
+            OL.row_stats(host[done % rows])
+            OL.log_softmax(host[done % rows])
+            done += 1
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": round(done / dt, 2), "unit": "tokens/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{done} rows of V={V} (row stats + log-softmax, fp64 numpy)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(ptg, cases, ws_bwds, streams, args, ws, flops_all):
     """Same metric, each step copying its inputs host->device from pinned
     memory and its outputs (O, dQ, dK, dV) device->host, through the same
@@ -578,6 +731,9 @@ def main(argv=None):
                          "load-balanced partitioner")
     ap.add_argument("--streams", type=int, default=2,
                     help="CUDA streams the independent tries of a batch alternate over")
+    ap.add_argument("--path", choices=["attention", "logprob"], default="attention",
+                    help="attention: the fwd+bwd step (default); logprob: the tree-aware "
+                         "log-prob / entropy gather over packed logits")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
@@ -588,6 +744,8 @@ def main(argv=None):
     rank, ws = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, ws)
+    elif args.path == "logprob":
+        run_logprob(args, rank, ws)
     else:
         run_ours(args, rank, ws)
     if ws > 1:

@@ -337,6 +337,99 @@ TREE_API tree_status_t tree_partition_sequences(const int32_t* tokens, const int
                                                 int64_t* max_cost);
 
 /* ------------------------------------------------------------------------
+ * tree_logprobs_entropy — log-probabilities and entropies of packed logits.
+ *
+ * Source: the guide's section "Log Probability 计算：树结构的特殊处理"
+ * (gather_packed_tree_logprobs_entropy and gather_packed_tree_vocab_stats).
+ * Row r of `logits` holds the next-token logits at packed token r.  Inside a
+ * node the row predicts the next token of the node; the last row of a node
+ * predicts the first token of each child (the page's transition).  So every
+ * real token j has one predicting row
+ *     pred(j) = the largest i < j with key_reach[i] >= j   (-1 if none),
+ * the last key before j that row j may attend to: j - 1 inside a node, the
+ * parent's last token at a node start, -1 at the start of a top-level node.
+ * Per row r (a real token):
+ *     lse[r]       = log sum_v exp(logits[r, v])
+ *     entropy[r]   = -sum_v p_v log p_v,  p = softmax(logits[r])
+ *     vocab_min[r] = min_v logits[r, v],  vocab_max[r] = max_v logits[r, v]
+ * Per token j:
+ *     logprob[j]    = logits[pred(j), token_ids[j]] - lse[pred(j)]  (0 if pred(j) < 0)
+ *     token_pred[j] = pred(j)
+ * Pads (key_reach[j] < j) get 0 everywhere and token_pred -1.  Every row's
+ * distribution is reduced once and every (pred, label) pair gathered once,
+ * which is what the page's per-node caches achieve.  fp32 arithmetic; the
+ * exponentials use the hardware 2^x approximation.  Logits are assumed to be
+ * finite: a -inf logit gives a NaN entropy (0 * log 0 in plain arithmetic),
+ * a NaN logit NaN results for its row.
+ *
+ *   logits        [in]  device [T_pad rows, row_stride elements], the first V
+ *                       of each row used; dtype TREE_DTYPE_BF16 or TREE_DTYPE_F32.
+ *                       Rows whose start is 16-byte aligned are read in
+ *                       16-byte groups, other layouts element by element.
+ *   token_ids     [in]  device int32[T_pad], the packed token ids (needed
+ *                       when logprob != NULL; pads may hold anything)
+ *   key_reach     [in]  device int32[T_pad] from tree_pack_positions
+ *   blockmap      [in]  from tree_blockmap_build for the same key_reach
+ *                       (needed when logprob or token_pred is requested)
+ *   lse           [out] device float[T_pad] (required)
+ *   entropy, vocab_min, vocab_max, logprob
+ *                 [out] device float[T_pad], each may be NULL to skip it
+ *   token_pred    [out] device int32[T_pad], may be NULL
+ *   dev_status    [out] TREE_ERR_MALFORMED_TREE if a token with a predicting
+ *                       row has an id outside [0, V) (its logprob is NaN)
+ * Returns TREE_ERR_UNSUPPORTED for another dtype, TREE_ERR_INVALID_ARG for a
+ * missing required pointer, V < 1 or row_stride < V, TREE_ERR_ALIGNMENT if
+ * T_pad % 128 != 0, TREE_ERR_WORKSPACE if blockmap_bytes is short.
+ * T_pad == 0 is a no-op (checked before the pointers).  Two launches (rows,
+ * then labels); one when neither logprob nor token_pred is requested.
+ * ---------------------------------------------------------------------- */
+typedef enum { TREE_DTYPE_BF16 = 0, TREE_DTYPE_F32 = 1 } tree_dtype_t;
+
+TREE_API tree_status_t tree_logprobs_entropy(const void* logits, int32_t dtype,
+                                             int64_t row_stride, int32_t T_pad, int32_t V,
+                                             const int32_t* token_ids, const int32_t* key_reach,
+                                             const void* blockmap, size_t blockmap_bytes,
+                                             float* lse, float* entropy, float* vocab_min,
+                                             float* vocab_max, float* logprob,
+                                             int32_t* token_pred, int32_t* dev_status,
+                                             tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * tree_merge_per_sequence — per-token results into a [n_seqs, max_len] batch.
+ *
+ * Source: the same section (merge_packed_tree_results: per-sequence results
+ * of several micro-batches put back into the original batch layout by
+ * sequence id, short sequences padded with padding_value).  Sequence s owns
+ * seq_pos[seq_offsets[s] .. seq_offsets[s+1]), the indices into `src` of its
+ * tokens in order (for several tries in one buffer: each trie's packed
+ * index plus the trie's offset).  With L its length:
+ *     out[s, t] = src[seq_pos[seq_offsets[s] + t + shift]]   for t < L - trim
+ *     out[s, t] = padding_value                              otherwise.
+ * Log-probabilities, which the token they score holds, use shift 1, trim 1
+ * (entry t scores token t+1).  Entropies and vocab statistics of the
+ * predicting rows use shift 0, trim 1.  Per-token values use 0, 0.
+ *
+ *   src          [in]  device float[n_src]
+ *   seq_pos      [in]  device int32[n_pos]
+ *   seq_offsets  [in]  device int64[n_seqs + 1], non-decreasing, last <= n_pos
+ *   out          [out] device float[n_seqs * max_len]
+ *   dev_status   [out] TREE_ERR_MALFORMED_TREE for an index outside [0, n_src)
+ *                      (that entry becomes NaN); TREE_ERR_INVALID_ARG for
+ *                      offsets that decrease or pass n_pos (the row is NaN);
+ *                      TREE_ERR_CAPACITY if L - trim > max_len.  As everywhere,
+ *                      after an error the outputs are undefined (blocks that
+ *                      start after it skip their work)
+ * Returns TREE_ERR_INVALID_ARG for negative sizes, shift < 0 or trim < shift,
+ * or a missing pointer.  n_seqs == 0 or max_len == 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+TREE_API tree_status_t tree_merge_per_sequence(const float* src, int64_t n_src,
+                                               const int32_t* seq_pos, int64_t n_pos,
+                                               const int64_t* seq_offsets, int32_t n_seqs,
+                                               int32_t max_len, int32_t shift, int32_t trim,
+                                               float padding_value, float* out,
+                                               int32_t* dev_status, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  *
  * tree_debug_wait_timeout — launch one warp that waits on a shared-memory

@@ -8,8 +8,10 @@ import fails loudly; build it with ``python prefix_tree_attention_gb300/build.py
 Entry points mirror the C ABI names: ``tree_pack_positions``,
 ``tree_blockmap_build``, ``tree_attn_fwd``, ``tree_attn_bwd`` (each takes
 tensors, checks their dtype/shape/device, passes raw pointers and the current
-CUDA stream, and raises ``TreeError`` on a non-OK status), plus the host
-packer ``pack_sequences``.
+CUDA stream, and raises ``TreeError`` on a non-OK status), the log-probability
+gather ``tree_logprobs_entropy`` with its merge ``tree_merge_per_sequence``,
+plus the host packer ``pack_sequences`` and partitioner
+``partition_sequences``.
 """
 from __future__ import annotations
 
@@ -56,6 +58,10 @@ _sig = {
     "tree_launch_count": (ctypes.c_uint64, []),
     "tree_pack_positions_noalloc": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P, _P, _P]),
     "tree_partition_sequences": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
+    "tree_logprobs_entropy": (ctypes.c_int, [_P, _I32, _I64, _I32, _I32, _P, _P, _P, _SZ, _P,
+                                             _P, _P, _P, _P, _P, _P, _P]),
+    "tree_merge_per_sequence": (ctypes.c_int, [_P, _I64, _P, _I64, _P, _I32, _I32, _I32, _I32,
+                                               _F32, _P, _P, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -195,6 +201,81 @@ def tree_attn_bwd(q, k, v, o, d_o, lse, key_reach, blockmap, dq, dk, dv, workspa
 
 def _nbytes(t) -> int:
     return t.numel() * t.element_size()
+
+
+DTYPE_BF16, DTYPE_F32 = 0, 1
+
+
+def tree_logprobs_entropy(logits, key_reach, lse, dev_status, token_ids=None, blockmap=None,
+                          entropy=None, vocab_min=None, vocab_max=None, logprob=None,
+                          token_pred=None, stream=None):
+    """Per-row log-sum-exp (and optionally entropy, vocab min/max) of packed
+    logits ``[T_pad, V]`` (bf16 or fp32, unit stride along V), and per token
+    the log-probability of its id under its predicting row and that row."""
+    import torch
+    if logits.dim() != 2 or logits.stride(1) != 1 or logits.device.type != "cuda":
+        raise ValueError("logits must be a 2-D CUDA tensor with unit stride along the vocabulary")
+    code = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32}.get(logits.dtype)
+    if code is None:
+        raise TypeError(f"logits must be bf16 or float32, got {logits.dtype}")
+    T_pad, V = logits.shape
+    _need(key_reach, torch.int32, "key_reach")
+    if key_reach.numel() != T_pad:
+        raise ValueError(f"key_reach must hold T_pad = {T_pad} values")
+    if blockmap is not None:
+        _need(blockmap, torch.int32, "blockmap")
+    for t, n in ((lse, "lse"), (entropy, "entropy"), (vocab_min, "vocab_min"),
+                 (vocab_max, "vocab_max"), (logprob, "logprob")):
+        if t is not None:
+            _need(t, torch.float32, n)
+            if t.numel() != T_pad:
+                raise ValueError(f"{n} must hold T_pad = {T_pad} values")
+    for t, n in ((token_ids, "token_ids"), (token_pred, "token_pred")):
+        if t is not None:
+            _need(t, torch.int32, n)
+            if t.numel() != T_pad:
+                raise ValueError(f"{n} must hold T_pad = {T_pad} values")
+    _check("tree_logprobs_entropy", _lib.tree_logprobs_entropy(
+        _ptr(logits), code, logits.stride(0), T_pad, V, _ptr(token_ids), _ptr(key_reach),
+        _ptr(blockmap), 0 if blockmap is None else _nbytes(blockmap), _ptr(lse), _ptr(entropy),
+        _ptr(vocab_min), _ptr(vocab_max), _ptr(logprob), _ptr(token_pred), _ptr(dev_status),
+        _stream_ptr(stream)))
+
+
+def tree_merge_per_sequence(src, seq_pos, seq_offsets, out, dev_status, shift: int, trim: int,
+                            padding_value: float = 0.0, stream=None):
+    """``out[s, t] = src[seq_pos[seq_offsets[s] + t + shift]]`` for
+    ``t < len(s) - trim``, else ``padding_value``; ``out`` is [n_seqs, max_len]."""
+    import torch
+    _need(src, torch.float32, "src")
+    _need(seq_pos, torch.int32, "seq_pos")
+    _need(seq_offsets, torch.int64, "seq_offsets")
+    _need(out, torch.float32, "out")
+    n_seqs, max_len = out.shape
+    if seq_offsets.numel() != n_seqs + 1:
+        raise ValueError("seq_offsets must hold n_seqs + 1 values")
+    _check("tree_merge_per_sequence", _lib.tree_merge_per_sequence(
+        _ptr(src), src.numel(), _ptr(seq_pos), seq_pos.numel(), _ptr(seq_offsets), n_seqs,
+        max_len, int(shift), int(trim), float(padding_value), _ptr(out), _ptr(dev_status),
+        _stream_ptr(stream)))
+
+
+def sequence_index_arrays(tries, n_seqs: int, trie_offsets=None):
+    """Host bookkeeping for ``tree_merge_per_sequence``: the packed indices
+    of every input sequence's tokens (plus its trie's offset in a buffer that
+    holds several tries), flattened in sequence-id order, and the int64
+    offsets of each sequence in that list."""
+    if trie_offsets is None:
+        trie_offsets = np.cumsum([0] + [t.T_pad for t in tries[:-1]]).tolist()
+    per = [None] * n_seqs
+    for t, base in zip(tries, trie_offsets):
+        for sid, idx in t.seq_index.items():
+            per[sid] = np.asarray(idx, np.int64) + int(base)
+    lens = np.array([0 if p is None else p.size for p in per], np.int64)
+    offs = np.zeros(n_seqs + 1, np.int64)
+    np.cumsum(lens, out=offs[1:])
+    flat = np.concatenate([p for p in per if p is not None]) if offs[-1] else np.zeros(0)
+    return flat.astype(np.int32), offs
 
 
 def tree_attn_bwd_prepare(o, d_o, lse, workspace, dev_status, stream=None):

@@ -1,0 +1,454 @@
+// tree_logprobs_entropy and tree_merge_per_sequence: log-probabilities and
+// entropies of packed next-token logits, and their per-sequence merge.
+//
+// AReaL Tree Training guide, section "Log Probability 计算：树结构的特殊处理".
+// A packed row's logits predict the next token of every sequence through it:
+// inside a node the next packed row, across a node boundary (the page's
+// transition from the parent's last row to a child's first token) every
+// child's first token.  So each real token j has one predicting row pred(j),
+// and the page's per-node caches become plain structure: every row's
+// distribution is reduced once, every (pred, label) pair is gathered once.
+//
+// pred(j) from the interval form of the mask, visible(i, j) <=> j <= i <=
+// reach[j]: pred(j) is the last key before j that row j sees, i.e. the
+// largest i < j with reach[i] >= j (-1 for the first token of a top-level
+// node).  It is j - 1 except at node starts, where the search skips the
+// subtrees of earlier siblings.  A key block b can hold pred(j) only if the
+// tile (block(j), b) is non-empty, i.e. col_hi[b] >= block(j) in the blockmap,
+// so whole blocks are skipped with one word.
+//
+// Kernels (each skips its work once *dev_status is non-zero):
+//  1 k_row_stats     one CTA per packed row: one streaming pass over the V
+//                    logits keeps a running max m, s = sum 2^u and
+//                    t = sum 2^u * u with u = (x - m) log2(e); then
+//                    lse = m + ln s and entropy = ln 2 * (log2 s - t / s)
+//                    (entropy = lse - sum p x, written relative to m).
+//                    HBM-bound: reads V logits per row once.
+//  2 k_label_lp      one thread per token: pred(j), then
+//                    logprob[j] = logits[pred(j), token_ids[j]] - lse[pred(j)].
+//  3 k_merge         one thread per output element of [n_seqs, max_len].
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace tree {
+namespace {
+
+constexpr int kRowThreads = 256;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kUnroll = 4;            // 16-byte loads in flight per thread
+constexpr int kLabelThreads = 128;
+constexpr int kMergeThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t min_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Running reduction of one row slice.  s and t are kept as two lanes each
+// so the per-element updates pair up into f32x2 instructions.
+struct Acc {
+  float m, s0, s1, t0, t1, mn;
+};
+
+__device__ __forceinline__ void acc_init(Acc& a) {
+  a.m = -INFINITY;
+  a.s0 = a.s1 = a.t0 = a.t1 = 0.f;
+  a.mn = INFINITY;
+}
+
+// Move the reference of (s, t) from a.m to m_new >= a.m:
+// u' = u + d with d = (a.m - m_new) log2(e), so s' = 2^d s and
+// t' = 2^d (t + d s).  Nothing accumulated yet (s == 0) needs no scaling.
+__device__ __forceinline__ void acc_rebase(Acc& a, float m_new) {
+  if (a.s0 + a.s1 > 0.f) {
+    const float d = (a.m - m_new) * kLog2e;
+    const float f = ex2f(d);
+    a.t0 = f * fmaf(d, a.s0, a.t0);
+    a.t1 = f * fmaf(d, a.s1, a.t1);
+    a.s0 *= f;
+    a.s1 *= f;
+  }
+  a.m = m_new;
+}
+
+// Two logits (x0, x1) at the current reference.
+__device__ __forceinline__ void acc_pair(Acc& a, float nmL, float x0, float x1) {
+  float u0, u1, e0, e1;
+  fma2(u0, u1, x0, x1, kLog2e, kLog2e, nmL, nmL);
+  e0 = ex2f(u0);
+  e1 = ex2f(u1);
+  fma2(a.t0, a.t1, e0, e1, u0, u1, a.t0, a.t1);
+  add2(a.s0, a.s1, a.s0, a.s1, e0, e1);
+}
+
+// One logit of the ragged tail or of an unaligned row.
+__device__ __forceinline__ void acc_one(Acc& a, float x) {
+  a.mn = fminf(a.mn, x);
+  if (x > a.m) acc_rebase(a, x);
+  const float u = fmaf(x, kLog2e, -a.m * kLog2e);
+  const float e = ex2f(u);
+  a.s0 += e;
+  a.t0 = fmaf(e, u, a.t0);
+}
+
+__device__ __forceinline__ void acc_merge(Acc& a, const Acc& b) {
+  Acc c = b;
+  const float m = fmaxf(a.m, c.m);
+  acc_rebase(a, m);
+  acc_rebase(c, m);
+  a.s0 = (a.s0 + a.s1) + (c.s0 + c.s1);
+  a.t0 = (a.t0 + a.t1) + (c.t0 + c.t1);
+  a.s1 = 0.f;
+  a.t1 = 0.f;
+  a.mn = fminf(a.mn, c.mn);
+}
+
+__device__ __forceinline__ Acc acc_shfl_xor(const Acc& a, int o) {
+  Acc b;
+  b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+  b.s0 = __shfl_xor_sync(0xffffffffu, a.s0, o);
+  b.s1 = __shfl_xor_sync(0xffffffffu, a.s1, o);
+  b.t0 = __shfl_xor_sync(0xffffffffu, a.t0, o);
+  b.t1 = __shfl_xor_sync(0xffffffffu, a.t1, o);
+  b.mn = __shfl_xor_sync(0xffffffffu, a.mn, o);
+  return b;
+}
+
+template <bool kBf16>
+__device__ __forceinline__ float load_logit(const void* row, int64_t e) {
+  if constexpr (kBf16) {
+    const uint16_t bits = reinterpret_cast<const uint16_t*>(row)[e];
+    return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+  } else {
+    return reinterpret_cast<const float*>(row)[e];
+  }
+}
+
+// A 16-byte group of logits at the current reference: 8 bf16 or 4 fp32.
+template <bool kBf16, bool kMin>
+__device__ __forceinline__ void acc_group_max(const uint4& v, uint32_t& mx_bf, float& mx_f,
+                                              uint32_t& mn_bf, float& mn_f) {
+  if constexpr (kBf16) {
+    mx_bf = max_bf16x2(max_bf16x2(mx_bf, max_bf16x2(v.x, v.y)), max_bf16x2(v.z, v.w));
+    if constexpr (kMin)
+      mn_bf = min_bf16x2(min_bf16x2(mn_bf, min_bf16x2(v.x, v.y)), min_bf16x2(v.z, v.w));
+  } else {
+    mx_f = fmaxf(fmaxf(mx_f, fmaxf(__uint_as_float(v.x), __uint_as_float(v.y))),
+                 fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    if constexpr (kMin)
+      mn_f = fminf(fminf(mn_f, fminf(__uint_as_float(v.x), __uint_as_float(v.y))),
+                   fminf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void acc_group(Acc& a, float nmL, const uint4& v) {
+  if constexpr (kBf16) {
+    acc_pair(a, nmL, bf_lo(v.x), bf_hi(v.x));
+    acc_pair(a, nmL, bf_lo(v.y), bf_hi(v.y));
+    acc_pair(a, nmL, bf_lo(v.z), bf_hi(v.z));
+    acc_pair(a, nmL, bf_lo(v.w), bf_hi(v.w));
+  } else {
+    acc_pair(a, nmL, __uint_as_float(v.x), __uint_as_float(v.y));
+    acc_pair(a, nmL, __uint_as_float(v.z), __uint_as_float(v.w));
+  }
+}
+
+// kVec: every row starts on a 16-byte boundary (checked on the host), so the
+// first V - V % W logits are read as 16-byte groups of W.
+template <bool kBf16, bool kVec, bool kMin>
+__global__ void __launch_bounds__(kRowThreads) k_row_stats(
+    const void* __restrict__ logits, int64_t row_stride, int32_t V,
+    const int32_t* __restrict__ reach, float* __restrict__ lse, float* __restrict__ entropy,
+    float* __restrict__ vmin, float* __restrict__ vmax, const int32_t* status) {
+  if (ld_status(status)) return;
+  const int32_t row = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (reach[row] < row) {            // pad token: no distribution
+    if (tid == 0) {
+      lse[row] = 0.f;
+      if (entropy) entropy[row] = 0.f;
+      if (vmin) vmin[row] = 0.f;
+      if (vmax) vmax[row] = 0.f;
+    }
+    return;
+  }
+  constexpr int kEsz = kBf16 ? 2 : 4;
+  constexpr int kW = 16 / kEsz;      // logits per 16-byte group
+  const char* base = reinterpret_cast<const char*>(logits) + row * row_stride * kEsz;
+  Acc a;
+  acc_init(a);
+  int64_t done = 0;
+  if constexpr (kVec) {
+    const uint4* g = reinterpret_cast<const uint4*>(base);
+    const int32_t ng = V / kW;
+    int32_t i = tid;
+    for (; i + (kUnroll - 1) * kRowThreads < ng; i += kUnroll * kRowThreads) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) v[u] = __ldcs(g + i + u * kRowThreads);
+      uint32_t mx_bf = 0xff80ff80u, mn_bf = 0x7f807f80u;   // (-inf, -inf), (+inf, +inf)
+      float mx_f = -INFINITY, mn_f = INFINITY;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) acc_group_max<kBf16, kMin>(v[u], mx_bf, mx_f, mn_bf, mn_f);
+      if constexpr (kBf16) {
+        mx_f = fmaxf(bf_lo(mx_bf), bf_hi(mx_bf));
+        if constexpr (kMin) mn_f = fminf(bf_lo(mn_bf), bf_hi(mn_bf));
+      }
+      if constexpr (kMin) a.mn = fminf(a.mn, mn_f);
+      if (mx_f > a.m) acc_rebase(a, mx_f);
+      const float nmL = -a.m * kLog2e;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) acc_group<kBf16>(a, nmL, v[u]);
+    }
+    for (; i < ng; i += kRowThreads) {
+      const uint4 v = __ldcs(g + i);
+      uint32_t mx_bf = 0xff80ff80u, mn_bf = 0x7f807f80u;
+      float mx_f = -INFINITY, mn_f = INFINITY;
+      acc_group_max<kBf16, kMin>(v, mx_bf, mx_f, mn_bf, mn_f);
+      if constexpr (kBf16) {
+        mx_f = fmaxf(bf_lo(mx_bf), bf_hi(mx_bf));
+        if constexpr (kMin) mn_f = fminf(bf_lo(mn_bf), bf_hi(mn_bf));
+      }
+      if constexpr (kMin) a.mn = fminf(a.mn, mn_f);
+      if (mx_f > a.m) acc_rebase(a, mx_f);
+      acc_group<kBf16>(a, -a.m * kLog2e, v);
+    }
+    done = static_cast<int64_t>(ng) * kW;
+  }
+  for (int64_t e = done + tid; e < V; e += kRowThreads) acc_one(a, load_logit<kBf16>(base, e));
+
+  // CTA reduction: warps by shuffles, then the warp leaders in warp 0.
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const Acc b = acc_shfl_xor(a, o);
+    acc_merge(a, b);
+  }
+  __shared__ Acc part[kRowWarps];
+  if ((tid & 31) == 0) part[tid >> 5] = a;
+  __syncthreads();
+  if (tid < 32) {
+    if (tid < kRowWarps) a = part[tid];
+    else acc_init(a);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const Acc b = acc_shfl_xor(a, o);
+      acc_merge(a, b);
+    }
+    if (tid == 0) {
+      const float s = a.s0 + a.s1, t = a.t0 + a.t1;
+      float l = -INFINITY, h = 0.f;
+      if (s > 0.f) {
+        const float l2s = log2f(s);
+        l = fmaf(kLn2, l2s, a.m);
+        h = kLn2 * (l2s - t / s);
+      }
+      lse[row] = l;
+      if (entropy) entropy[row] = h;
+      if (vmin) vmin[row] = a.mn;
+      if (vmax) vmax[row] = a.m;
+    }
+  }
+}
+
+// Largest i < q with reach[i] >= q (q - 1 is known to fail), or -1.
+// Called by all 32 lanes of a warp with the same q; returns the same value
+// on every lane.
+__device__ int32_t find_pred(int32_t q, const int32_t* __restrict__ reach,
+                             const int32_t* __restrict__ col_hi, int lane) {
+  const int32_t qb = q >> 7;
+  const int32_t lo = qb << 7;
+  for (int32_t top = q - 2; top >= lo; top -= 32) {        // q's own block
+    const int32_t i = top - lane;
+    const bool hit = i >= lo && reach[i] >= q;
+    const uint32_t b = __ballot_sync(0xffffffffu, hit);
+    if (b) return top - (__ffs(b) - 1);
+  }
+  for (int32_t btop = qb - 1; btop >= 0; btop -= 32) {     // earlier blocks
+    const int32_t bl = btop - lane;
+    const bool cand = bl >= 0 && col_hi[bl] >= qb;
+    uint32_t cb = __ballot_sync(0xffffffffu, cand);
+    while (cb) {
+      const int l = __ffs(cb) - 1;
+      cb &= cb - 1;
+      const int32_t blk = btop - l;                        // highest block first
+      for (int w = 0; w < kBlock / 32; ++w) {
+        const int32_t top = blk * kBlock + kBlock - 1 - w * 32;
+        const uint32_t b = __ballot_sync(0xffffffffu, reach[top - lane] >= q);
+        if (b) return top - (__ffs(b) - 1);
+      }
+    }
+  }
+  return -1;
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kLabelThreads) k_label_lp(
+    const void* __restrict__ logits, int64_t row_stride, int32_t V,
+    const int32_t* __restrict__ token_ids, const int32_t* __restrict__ reach,
+    BlockmapView bm, const float* __restrict__ lse, float* __restrict__ logprob,
+    int32_t* __restrict__ pred_out, int32_t* status) {
+  if (ld_status(status)) return;
+  const int32_t j = blockIdx.x * kLabelThreads + threadIdx.x;   // T_pad % 128 == 0
+  const int lane = threadIdx.x & 31;
+  const bool real = reach[j] >= j;
+  int32_t pred = -1;
+  bool slow = false;
+  if (real && j > 0) {
+    if (reach[j - 1] >= j) pred = j - 1;
+    else slow = true;
+  }
+  uint32_t pend = __ballot_sync(0xffffffffu, slow);
+  while (pend) {
+    const int src = __ffs(pend) - 1;
+    pend &= pend - 1;
+    const int32_t q = __shfl_sync(0xffffffffu, j, src);
+    const int32_t found = find_pred(q, reach, bm.col_hi(), lane);
+    if (lane == src) pred = found;
+  }
+  if (pred_out) pred_out[j] = pred;
+  if (logprob) {
+    float out = 0.f;
+    if (pred >= 0) {
+      const int32_t tok = token_ids[j];
+      if (tok < 0 || tok >= V) {
+        set_status(status, TREE_ERR_MALFORMED_TREE);
+        out = __int_as_float(0x7fc00000);
+      } else {
+        constexpr int kEsz = kBf16 ? 2 : 4;
+        const char* row = reinterpret_cast<const char*>(logits) + pred * row_stride * kEsz;
+        out = load_logit<kBf16>(row, tok) - lse[pred];
+      }
+    }
+    logprob[j] = out;
+  }
+}
+
+__global__ void __launch_bounds__(kMergeThreads) k_merge(
+    const float* __restrict__ src, int64_t n_src, const int32_t* __restrict__ seq_pos,
+    int64_t n_pos, const int64_t* __restrict__ seq_off, int32_t n_seqs, int32_t max_len,
+    int32_t shift, int32_t trim, float pad, float* __restrict__ out, int32_t* status) {
+  if (ld_status(status)) return;
+  const int32_t t = blockIdx.x * kMergeThreads + threadIdx.x;
+  if (t >= max_len) return;
+  for (int32_t s = blockIdx.y; s < n_seqs; s += gridDim.y) {
+    const int64_t off = seq_off[s], end = seq_off[s + 1];
+    const int64_t n = end - off - trim;              // entries of sequence s
+    float v = pad;
+    if (off < 0 || end < off || end > n_pos) {
+      set_status(status, TREE_ERR_INVALID_ARG);
+      v = __int_as_float(0x7fc00000);
+    } else if (t < n) {
+      const int32_t p = seq_pos[off + t + shift];
+      if (p < 0 || p >= n_src) {
+        set_status(status, TREE_ERR_MALFORMED_TREE);
+        v = __int_as_float(0x7fc00000);
+      } else {
+        v = src[p];
+      }
+    }
+    if (t == 0 && n > max_len) set_status(status, TREE_ERR_CAPACITY);
+    out[static_cast<int64_t>(s) * max_len + t] = v;
+  }
+}
+
+template <bool kBf16>
+cudaError_t launch_stats(const void* logits, int64_t stride, int32_t T_pad, int32_t V, bool vec,
+                         const int32_t* reach, float* lse, float* ent, float* vmin, float* vmax,
+                         int32_t* status, cudaStream_t s) {
+  const dim3 grid(T_pad), block(kRowThreads);
+  const bool want_min = vmin != nullptr;
+  if (vec && want_min)
+    k_row_stats<kBf16, true, true><<<grid, block, 0, s>>>(logits, stride, V, reach, lse, ent,
+                                                          vmin, vmax, status);
+  else if (vec)
+    k_row_stats<kBf16, true, false><<<grid, block, 0, s>>>(logits, stride, V, reach, lse, ent,
+                                                           vmin, vmax, status);
+  else if (want_min)
+    k_row_stats<kBf16, false, true><<<grid, block, 0, s>>>(logits, stride, V, reach, lse, ent,
+                                                           vmin, vmax, status);
+  else
+    k_row_stats<kBf16, false, false><<<grid, block, 0, s>>>(logits, stride, V, reach, lse, ent,
+                                                            vmin, vmax, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace tree
+
+extern "C" {
+
+tree_status_t tree_logprobs_entropy(const void* logits, int32_t dtype, int64_t row_stride,
+                                    int32_t T_pad, int32_t V, const int32_t* token_ids,
+                                    const int32_t* key_reach, const void* blockmap,
+                                    size_t blockmap_bytes, float* lse, float* entropy,
+                                    float* vocab_min, float* vocab_max, float* logprob,
+                                    int32_t* token_pred, int32_t* dev_status,
+                                    tree_stream_t stream) {
+  using namespace tree;
+  if (dtype != TREE_DTYPE_BF16 && dtype != TREE_DTYPE_F32) return TREE_ERR_UNSUPPORTED;
+  if (T_pad < 0 || V < 1 || row_stride < V) return TREE_ERR_INVALID_ARG;
+  if (T_pad % kBlock) return TREE_ERR_ALIGNMENT;
+  if (T_pad == 0) return TREE_OK;
+  if (!logits || !key_reach || !lse || !dev_status) return TREE_ERR_INVALID_ARG;
+  const bool labels = logprob != nullptr || token_pred != nullptr;
+  if (labels && !blockmap) return TREE_ERR_INVALID_ARG;
+  if (logprob && !token_ids) return TREE_ERR_INVALID_ARG;
+  if (labels && blockmap_bytes < tree_blockmap_bytes(T_pad)) return TREE_ERR_WORKSPACE;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf16 = dtype == TREE_DTYPE_BF16;
+  const int64_t esz = bf16 ? 2 : 4;
+  const bool vec = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && (row_stride * esz) % 16 == 0;
+  cudaError_t e = bf16 ? launch_stats<true>(logits, row_stride, T_pad, V, vec, key_reach, lse,
+                                            entropy, vocab_min, vocab_max, dev_status, s)
+                       : launch_stats<false>(logits, row_stride, T_pad, V, vec, key_reach, lse,
+                                             entropy, vocab_min, vocab_max, dev_status, s);
+  count_launches(1);
+  if (e != cudaSuccess) return TREE_ERR_CUDA;
+  if (labels) {
+    BlockmapView bm{T_pad / kBlock,
+                    static_cast<int32_t*>(const_cast<void*>(blockmap))};
+    const dim3 grid(T_pad / kLabelThreads), block(kLabelThreads);
+    if (bf16)
+      k_label_lp<true><<<grid, block, 0, s>>>(logits, row_stride, V, token_ids, key_reach, bm,
+                                              lse, logprob, token_pred, dev_status);
+    else
+      k_label_lp<false><<<grid, block, 0, s>>>(logits, row_stride, V, token_ids, key_reach, bm,
+                                               lse, logprob, token_pred, dev_status);
+    count_launches(1);
+    if (cudaGetLastError() != cudaSuccess) return TREE_ERR_CUDA;
+  }
+  return TREE_OK;
+}
+
+tree_status_t tree_merge_per_sequence(const float* src, int64_t n_src, const int32_t* seq_pos,
+                                      int64_t n_pos, const int64_t* seq_offsets, int32_t n_seqs,
+                                      int32_t max_len, int32_t shift, int32_t trim,
+                                      float padding_value, float* out, int32_t* dev_status,
+                                      tree_stream_t stream) {
+  using namespace tree;
+  if (n_seqs < 0 || max_len < 0 || n_src < 0 || n_pos < 0 || shift < 0 || trim < shift)
+    return TREE_ERR_INVALID_ARG;
+  if (n_seqs == 0 || max_len == 0) return TREE_OK;
+  if (!src || !seq_pos || !seq_offsets || !out || !dev_status) return TREE_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid((max_len + kMergeThreads - 1) / kMergeThreads, n_seqs < 65535 ? n_seqs : 65535);
+  k_merge<<<grid, kMergeThreads, 0, s>>>(src, n_src, seq_pos, n_pos, seq_offsets, n_seqs, max_len,
+                                         shift, trim, padding_value, out, dev_status);
+  count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? TREE_OK : TREE_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -92,6 +92,46 @@ def test_host_side_errors_return_before_launch():
               None) == 1
 
 
+
+def test_logprob_entry_points_check_arguments_before_launch():
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    f = lib.tree_logprobs_entropy
+    f.restype = ctypes.c_int
+    f.argtypes = [P, I32, I64, I32, I32, P, P, P, SZ, P, P, P, P, P, P, P, P]
+
+    def call(dtype=0, stride=1000, T=256, V=1000, tok=FAKE, bm=FAKE, bm_bytes=1 << 20,
+             lse=FAKE, logprob=FAKE, pred=None, logits=FAKE):
+        return f(logits, dtype, stride, T, V, tok, FAKE, bm, bm_bytes, lse, None, None, None,
+                 logprob, pred, FAKE, None)
+    assert call(dtype=2) == 5                    # dtype other than bf16 / fp32
+    assert call(V=0) == 1 and call(stride=999) == 1
+    assert call(T=200) == 2                      # T_pad not a multiple of 128
+    assert call(logits=None) == 1 and call(lse=None) == 1
+    assert call(bm=None) == 1                    # labels need the blockmap
+    assert call(tok=None) == 1                   # logprob needs token ids
+    assert call(bm_bytes=16) == 8                # blockmap buffer too small
+    assert call(T=0) == 0 and call(T=0, logits=None) == 0   # empty input is a no-op
+    m = lib.tree_merge_per_sequence
+    m.restype = ctypes.c_int
+    m.argtypes = [P, I64, P, I64, P, I32, I32, I32, I32, ctypes.c_float, P, P, P]
+    assert m(FAKE, 10, FAKE, 10, FAKE, 2, 8, 1, 0, 0.0, FAKE, FAKE, None) == 1   # trim < shift
+    assert m(FAKE, 10, FAKE, 10, FAKE, 2, 8, -1, 0, 0.0, FAKE, FAKE, None) == 1
+    assert m(FAKE, -1, FAKE, 10, FAKE, 2, 8, 1, 1, 0.0, FAKE, FAKE, None) == 1
+    assert m(None, 10, FAKE, 10, FAKE, 2, 8, 1, 1, 0.0, FAKE, FAKE, None) == 1
+    assert m(FAKE, 10, FAKE, 10, FAKE, 0, 8, 1, 1, 0.0, FAKE, FAKE, None) == 0   # no-op
+
+
+def test_sequence_index_arrays_layout():
+    tries = ptg.pack_sequences([[1, 2, 3], [1, 2, 4, 5], [7]], 128)
+    pos, offs = ptg.sequence_index_arrays(tries, 3)
+    assert offs.tolist() == [0, 3, 7, 8]
+    for sid, L in enumerate((3, 4, 1)):
+        t = next(t for t in tries if sid in t.seq_index)
+        base = sum(u.T_pad for u in tries[:tries.index(t)])
+        assert pos[offs[sid]:offs[sid + 1]].tolist() == (t.seq_index[sid] + base).tolist()
+        assert offs[sid + 1] - offs[sid] == L
+
+
 def _same_packing(mine, ref):
     assert len(mine) == len(ref)
     for a, b in zip(mine, ref):

@@ -21,7 +21,9 @@ Sources (web pages; cited by title and section):
 * "AREAL-DTA: Dynamic Tree Attention for Efficient Reinforcement Learning of
   Large Language Models", section 3 "Problem formalisation" (total loss is the
   sum of per-sequence losses; a shared prefix is computed once and its
-  gradient sums the contributions of every descendant sequence) and section 4
+  gradient sums the contributions of every descendant sequence), sections
+  3.1-3.2 (depth-first traversal with a key/value stack, chunked backward,
+  no leaf KV caching, greedy DFS order) and section 4
   "负载均衡并行化" (load-balanced split of a batch over training workers).
 
 Modules:
@@ -33,6 +35,9 @@ Modules:
 * ``oracle.attention`` — masked softmax attention forward/backward in fp64.
 * ``oracle.partition`` — prefix-tree token cost and the optimal contiguous
                          split of the DFS order over K workers.
+* ``oracle.dta``       — the depth-first traversal schedule of dynamic tree
+                         attention (push / leaf / pop ops over chunks) and
+                         attention executed through it with a KV stack.
 * ``oracle.logprob``   — node-internal and transition log-probabilities,
                          entropies and vocabulary min/max of packed logits,
                          and the per-sequence merge.

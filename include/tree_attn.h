@@ -430,6 +430,52 @@ TREE_API tree_status_t tree_merge_per_sequence(const float* src, int64_t n_src,
                                                int32_t* dev_status, tree_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * tree_dta_schedule — the depth-first traversal of dynamic tree attention.
+ *
+ * Source: AREAL-DTA, sections 3.1 (DFS over the prefix tree with a stack of
+ * the current path's keys/values: forward and push on the way down, the
+ * leaf's backward as soon as its sequence is complete, a node's backward
+ * when it is popped, after all its descendants) and 3.2 (chunks of at most
+ * `chunk` tokens, 2048 on the page; a leaf's last chunk is never pushed; a
+ * greedy DFS order).  Readings: chunks cut each node's span every `chunk`
+ * tokens from its first token; children are visited deepest first (longest
+ * continuation in tokens below the child's first token), ties by preorder
+ * rank.  The op list, one int32 triple (kind, t0, t1) per op over packed rows
+ * [t0, t1):
+ *   TREE_DTA_FWD_PUSH  forward of the rows against the stack, then push them
+ *   TREE_DTA_FWD_BWD   a leaf's last chunk: forward and backward, no push
+ *   TREE_DTA_BWD_POP   backward of the rows on top of the stack, then pop
+ * At every forward the stack holds exactly the rows' ancestor tokens, so
+ * each op is the packed tree attention restricted to its query rows; every
+ * real token gets one forward and one backward; a token's backward comes
+ * after those of all rows that see it.
+ *
+ *   token_node, node_entry, node_exit  [in]  host arrays, as for
+ *                       tree_pack_positions (T_pad a multiple of 128)
+ *   chunk          [in]  >= 1
+ *   ops            [out] host int32[capacity][3], may be NULL to count only
+ *   n_ops          [out] number of ops (always written)
+ *   peak_stack_tokens [out] largest number of tokens on the stack (may be NULL)
+ * Returns TREE_ERR_INVALID_ARG (bad sizes, chunk < 1, missing pointer),
+ * TREE_ERR_ALIGNMENT (T_pad % 128), TREE_ERR_MALFORMED_TREE (node id out of
+ * range, empty or split node, ranks not a permutation, nodes not in rank
+ * order, crossing subtree intervals), TREE_ERR_WORKSPACE when ops is given
+ * and capacity < n_ops (the first `capacity` ops are written).  Pure host
+ * code; no device work.
+ * ---------------------------------------------------------------------- */
+typedef enum {
+  TREE_DTA_FWD_PUSH = 0,
+  TREE_DTA_FWD_BWD = 1,
+  TREE_DTA_BWD_POP = 2
+} tree_dta_op_t;
+
+TREE_API tree_status_t tree_dta_schedule(const int32_t* token_node, int32_t T_pad,
+                                         const int32_t* node_entry, const int32_t* node_exit,
+                                         int32_t n_nodes, int32_t chunk, int32_t* ops,
+                                         int64_t capacity, int64_t* n_ops,
+                                         int64_t* peak_stack_tokens);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  *
  * tree_debug_wait_timeout — launch one warp that waits on a shared-memory

@@ -10,8 +10,8 @@ Entry points mirror the C ABI names: ``tree_pack_positions``,
 tensors, checks their dtype/shape/device, passes raw pointers and the current
 CUDA stream, and raises ``TreeError`` on a non-OK status), the log-probability
 gather ``tree_logprobs_entropy`` with its merge ``tree_merge_per_sequence``,
-plus the host packer ``pack_sequences`` and partitioner
-``partition_sequences``.
+plus the host packer ``pack_sequences``, partitioner ``partition_sequences``
+and the DFS traversal schedule ``dta_schedule``.
 """
 from __future__ import annotations
 
@@ -62,6 +62,7 @@ _sig = {
                                              _P, _P, _P, _P, _P, _P, _P]),
     "tree_merge_per_sequence": (ctypes.c_int, [_P, _I64, _P, _I64, _P, _I32, _I32, _I32, _I32,
                                                _F32, _P, _P, _P]),
+    "tree_dta_schedule": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -258,6 +259,27 @@ def tree_merge_per_sequence(src, seq_pos, seq_offsets, out, dev_status, shift: i
         _ptr(src), src.numel(), _ptr(seq_pos), seq_pos.numel(), _ptr(seq_offsets), n_seqs,
         max_len, int(shift), int(trim), float(padding_value), _ptr(out), _ptr(dev_status),
         _stream_ptr(stream)))
+
+
+DTA_FWD_PUSH, DTA_FWD_BWD, DTA_BWD_POP = 0, 1, 2
+
+
+def dta_schedule(token_node, node_entry, node_exit, chunk: int = 2048):
+    """The depth-first traversal of dynamic tree attention for one packed
+    trie (host arrays): returns ``(ops, peak_stack_tokens)`` with ``ops`` an
+    int32 array ``[n_ops, 3]`` of ``(kind, t0, t1)``."""
+    tn = np.ascontiguousarray(token_node, dtype=np.int32)
+    en = np.ascontiguousarray(node_entry, dtype=np.int32)
+    ex = np.ascontiguousarray(node_exit, dtype=np.int32)
+    n_ops, peak = ctypes.c_int64(), ctypes.c_int64()
+    args = (tn.ctypes.data if tn.size else None, tn.size, en.ctypes.data if en.size else None,
+            ex.ctypes.data if ex.size else None, en.size, int(chunk))
+    _check("tree_dta_schedule", _lib.tree_dta_schedule(*args, None, 0, ctypes.byref(n_ops),
+                                                       ctypes.byref(peak)))
+    ops = np.zeros((max(1, n_ops.value), 3), np.int32)
+    _check("tree_dta_schedule", _lib.tree_dta_schedule(*args, ops.ctypes.data, n_ops.value,
+                                                       ctypes.byref(n_ops), ctypes.byref(peak)))
+    return ops[:n_ops.value], int(peak.value)
 
 
 def sequence_index_arrays(tries, n_seqs: int, trie_offsets=None):

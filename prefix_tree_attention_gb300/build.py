@@ -23,7 +23,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 CUDA_SOURCES = ["api.cu", "positions.cu", "blockmap.cu", "attn_fwd.cu", "attn_bwd.cu",
                 "diag.cu", "logprob.cu"]
-CXX_SOURCES = ["packer.cpp", "partition.cpp"]
+CXX_SOURCES = ["packer.cpp", "partition.cpp", "dta.cpp"]
 
 
 def _nvcc() -> str:

@@ -20,7 +20,7 @@ attention operator:
 * 3.2 "optimal DFS order": a greedy order that favours long uninterrupted
   push/pop runs.
 
-Readings where the page is silent (each stated again in the design doc):
+Readings where the page is silent:
 * chunks cut each node's token span from the node's first token, every
   ``chunk`` tokens (a node shorter than ``chunk`` is one chunk);
 * the greedy order visits a node's children by decreasing depth in tokens
@@ -51,8 +51,8 @@ import numpy as np
 FWD_PUSH, FWD_BWD, BWD_POP = 0, 1, 2
 
 
-def children(packed) -> list[list[int]]:
-    """Children of every node in preorder rank; index -1 -> top-level nodes."""
+def children(packed) -> tuple[list[list[int]], list[int]]:
+    """(children of every node, top-level nodes), each list in preorder rank."""
     kids: list[list[int]] = [[] for _ in range(packed.n_nodes)]
     top: list[int] = []
     for n in sorted(range(packed.n_nodes), key=lambda n: int(packed.node_entry[n])):

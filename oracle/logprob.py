@@ -22,7 +22,7 @@ statistics (``gather_packed_tree_vocab_stats``) and the merge of per-sequence
 results of several micro-batches back into a ``[batch, max_len]`` layout
 padded with ``padding_value`` (``merge_packed_tree_results``).
 
-Readings where the page is silent (each stated again in the design doc):
+Readings where the page is silent:
 * the input is the packed logits ``[T_pad, V]`` (one row per packed token);
   log-softmax is the plain definition ``x - logsumexp(x)`` in float64 on the
   given values, with no temperature;

@@ -19,7 +19,7 @@ Validation follows section "参数背后的源码校验逻辑": ``max_tokens_per
 must be positive and a multiple of the block, and no sequence may be longer
 than ``max_tokens_per_mb``.
 
-Readings where the page is silent (each stated again in the design doc):
+Readings where the page is silent:
 * children keep insertion order (the page keys children in a ``dict``);
 * FFD sorts by length descending, ties by original index (stable sort);
 * capacity counts uncompressed nodes, i.e. tokens;

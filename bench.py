@@ -225,8 +225,52 @@ def oracle_sample(key: str, seed: int, budget_s: float, tensors_fn=None):
     return flops / dt / 1e12, desc, dt, torch.get_num_threads()
 
 
+def logprob_oracle_rate(budget_s: float, seed: int, rows: int = 64, V: int = 151936):
+    """Time the log-prob oracle (as it stands) on host rows of bf16 logits over
+    the Qwen3 vocabulary: per row its statistics (log-sum-exp, entropy, vocab
+    min/max) and its log-softmax, which is what every packed token costs.
+    Returns (rows per second, description)."""
+    from oracle import logprob as OL
+    host = W.logits(rows, V, seed=seed).float().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        OL.row_stats(host[done % rows])
+        OL.log_softmax(host[done % rows])
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, f"{done} rows of V={V} (row stats + log-softmax, fp64 numpy, one core)"
+
+
+def run_reference_logprob(args):
+    budget = min(args.cpu_budget, 10.0)
+    vals, desc = [], None
+    for step in range(args.warmup + args.steps):
+        v, desc = logprob_oracle_rate(budget, args.seed)
+        if step >= args.warmup:
+            vals.append(v)
+    value = round(float(np.median(vals)), 2)
+    line = {
+        "impl": "reference", "metric": LOGPROB_METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "path": "logprob", "vocab": 151936},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, ws):
     if rank != 0:
+        return
+    if args.path == "logprob":
+        run_reference_logprob(args)
         return
     budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
     vals = []
@@ -486,7 +530,6 @@ def run_logprob(args, rank, ws):
     """
     import torch
     import prefix_tree_attention_gb300 as ptg
-    from oracle import logprob as OL
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -602,19 +645,9 @@ def run_logprob(args, rank, ws):
         "e2e": None,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        # the oracle's row reduction and label gather on host rows of the same logits
-        rows = min(64, tries[0].n_tokens)
-        host = logits[:rows].float().cpu().numpy().astype(np.float64)
-        t0 = time.perf_counter()
-        done = 0
-        while time.perf_counter() - t0 < min(args.cpu_budget, 10.0):
-            OL.row_stats(host[done % rows])
-            OL.log_softmax(host[done % rows])
-            done += 1
-        dt = time.perf_counter() - t0
-        line["cpu_baseline"] = {"value": round(done / dt, 2), "unit": "tokens/s", "cores": 1,
-                                "kind": "oracle",
-                                "sample": f"{done} rows of V={V} (row stats + log-softmax, fp64 numpy)"}
+        rate, desc = logprob_oracle_rate(min(args.cpu_budget, 10.0), seed)
+        line["cpu_baseline"] = {"value": round(rate, 2), "unit": "tokens/s", "cores": 1,
+                                "kind": "oracle", "sample": desc}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

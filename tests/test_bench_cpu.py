@@ -30,6 +30,19 @@ def test_reference_arm_prints_one_json_line():
     assert rec["config"]["workload"] == "tiny"
 
 
+def test_reference_arm_logprob_path():
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--path", "logprob", "--steps", "1", "--warmup", "0",
+                    "--cpu-budget", "0.5"])
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["metric"] == bench.LOGPROB_METRIC
+    assert rec["unit"] == "tokens/s" and rec["value"] > 0
+    assert rec["cpu_baseline"]["kind"] == "oracle" and rec["config"]["path"] == "logprob"
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))

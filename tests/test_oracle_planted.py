@@ -12,10 +12,12 @@ import test_oracle_attention as TA
 import test_oracle_dta as TD
 import test_oracle_logprob as TL
 import test_oracle_trie as TT
+import test_partition as TP
 from oracle import attention as OA
 from oracle import dta as OD
 from oracle import logprob as OL
 from oracle import mask as OM
+from oracle import partition as OP
 from oracle import trie as OT
 
 
@@ -217,3 +219,30 @@ def test_unmodified_schedule_variant_passes(monkeypatch):
     monkeypatch.setattr(OD, "schedule", _schedule_variant())
     TD.test_worked_example_schedules()
     TD.test_structure_random_tries(3)
+
+
+# ------------------------------------------------------------ partitioner
+def test_tree_tokens_without_sharing_is_caught(monkeypatch):
+    monkeypatch.setattr(OP, "tree_tokens", lambda group: sum(len(s) for s in group))
+    with pytest.raises(AssertionError):
+        TP.test_tree_tokens_worked_example()
+
+
+def test_dp_that_forgets_the_last_segment_is_caught(monkeypatch):
+    def optimal_drop_last(seqs, n_groups):
+        order = OP.dfs_order(seqs)
+        n = len(order)
+        inf = float("inf")
+        best = [[inf] * (n + 1) for _ in range(n_groups + 1)]
+        best[0][0] = 0
+        for k in range(1, n_groups + 1):
+            for j in range(1, n + 1):
+                for i in range(k - 1, j):
+                    if best[k - 1][i] == inf:
+                        continue
+                    c = OP.tree_tokens([seqs[order[t]] for t in range(i, j)])
+                    best[k][j] = min(best[k][j], best[k - 1][i] if k > 1 else c)
+        return int(min(best[k][n] for k in range(1, n_groups + 1)))
+    monkeypatch.setattr(OP, "optimal_contiguous", optimal_drop_last)
+    with pytest.raises(AssertionError):
+        TP.test_optimal_contiguous_equals_exhaustive_enumeration()

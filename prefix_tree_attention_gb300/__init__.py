@@ -117,6 +117,14 @@ def _need(t, dtype, name):
     del torch
 
 
+def _on_device(**tensors):
+    """Every tensor handed to a device entry point must live on a CUDA device:
+    a host pointer reaching a kernel would fault, and there is no CPU path."""
+    for name, t in tensors.items():
+        if t is not None and t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor")
+
+
 # --------------------------------------------------------------- workspaces
 def pack_positions_workspace_bytes(T_pad: int, n_nodes: int) -> int:
     return int(_lib.tree_pack_positions_workspace_bytes(T_pad, n_nodes))
@@ -134,6 +142,9 @@ def attn_bwd_workspace_bytes(T_pad: int, Hq: int, d: int) -> int:
 def tree_pack_positions(token_node, node_entry, node_exit, position_ids, key_reach, workspace,
                         dev_status, stream=None):
     import torch
+    _on_device(token_node=token_node, node_entry=node_entry, node_exit=node_exit,
+               position_ids=position_ids, key_reach=key_reach, workspace=workspace,
+               dev_status=dev_status)
     _need(token_node, torch.int32, "token_node")
     for t, n in ((position_ids, "position_ids"), (key_reach, "key_reach")):
         _need(t, torch.int32, n)
@@ -150,6 +161,8 @@ def tree_pack_positions_noalloc(token_node, node_entry, node_exit, position_ids,
     """tree_pack_positions with the library's fixed device scratch array
     (no workspace argument; T_pad and n_nodes up to 65536)."""
     import torch
+    _on_device(token_node=token_node, node_entry=node_entry, node_exit=node_exit,
+               position_ids=position_ids, key_reach=key_reach, dev_status=dev_status)
     _need(token_node, torch.int32, "token_node")
     for t, n in ((position_ids, "position_ids"), (key_reach, "key_reach")):
         _need(t, torch.int32, n)
@@ -162,6 +175,7 @@ def tree_pack_positions_noalloc(token_node, node_entry, node_exit, position_ids,
 
 def tree_blockmap_build(key_reach, blockmap, dev_status, stream=None, block: int = BLOCK):
     import torch
+    _on_device(key_reach=key_reach, blockmap=blockmap, dev_status=dev_status)
     _need(key_reach, torch.int32, "key_reach")
     _check("tree_blockmap_build", _lib.tree_blockmap_build(
         _ptr(key_reach), key_reach.numel(), block, _ptr(blockmap),
@@ -170,6 +184,8 @@ def tree_blockmap_build(key_reach, blockmap, dev_status, stream=None, block: int
 
 def tree_attn_fwd(q, k, v, key_reach, blockmap, o, lse, dev_status, scale=None, stream=None):
     import torch
+    _on_device(q=q, k=k, v=v, key_reach=key_reach, blockmap=blockmap, o=o, lse=lse,
+               dev_status=dev_status)
     T, Hq, d = q.shape
     Hkv = k.shape[1]
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
@@ -186,6 +202,8 @@ def tree_attn_fwd(q, k, v, key_reach, blockmap, o, lse, dev_status, scale=None, 
 def tree_attn_bwd(q, k, v, o, d_o, lse, key_reach, blockmap, dq, dk, dv, workspace, dev_status,
                   scale=None, stream=None):
     import torch
+    _on_device(q=q, k=k, v=v, o=o, d_o=d_o, lse=lse, key_reach=key_reach, blockmap=blockmap,
+               dq=dq, dk=dk, dv=dv, workspace=workspace, dev_status=dev_status)
     T, Hq, d = q.shape
     Hkv = k.shape[1]
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (d_o, "d_o"), (dq, "dq"), (dk, "dk"),
@@ -214,6 +232,9 @@ def tree_logprobs_entropy(logits, key_reach, lse, dev_status, token_ids=None, bl
     logits ``[T_pad, V]`` (bf16 or fp32, unit stride along V), and per token
     the log-probability of its id under its predicting row and that row."""
     import torch
+    _on_device(logits=logits, key_reach=key_reach, lse=lse, dev_status=dev_status,
+               token_ids=token_ids, blockmap=blockmap, entropy=entropy, vocab_min=vocab_min,
+               vocab_max=vocab_max, logprob=logprob, token_pred=token_pred)
     if logits.dim() != 2 or logits.stride(1) != 1 or logits.device.type != "cuda":
         raise ValueError("logits must be a 2-D CUDA tensor with unit stride along the vocabulary")
     code = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32}.get(logits.dtype)
@@ -248,6 +269,7 @@ def tree_merge_per_sequence(src, seq_pos, seq_offsets, out, dev_status, shift: i
     """``out[s, t] = src[seq_pos[seq_offsets[s] + t + shift]]`` for
     ``t < len(s) - trim``, else ``padding_value``; ``out`` is [n_seqs, max_len]."""
     import torch
+    _on_device(src=src, seq_pos=seq_pos, seq_offsets=seq_offsets, out=out, dev_status=dev_status)
     _need(src, torch.float32, "src")
     _need(seq_pos, torch.int32, "seq_pos")
     _need(seq_offsets, torch.int64, "seq_offsets")
@@ -301,6 +323,7 @@ def sequence_index_arrays(tries, n_seqs: int, trie_offsets=None):
 
 
 def tree_attn_bwd_prepare(o, d_o, lse, workspace, dev_status, stream=None):
+    _on_device(o=o, d_o=d_o, lse=lse, workspace=workspace, dev_status=dev_status)
     T, Hq, d = o.shape
     _check("tree_attn_bwd_prepare", _lib.tree_attn_bwd_prepare(
         _ptr(o), _ptr(d_o), _ptr(lse), T, Hq, d, _ptr(workspace), _nbytes(workspace),
@@ -309,6 +332,8 @@ def tree_attn_bwd_prepare(o, d_o, lse, workspace, dev_status, stream=None):
 
 def tree_attn_bwd_main(q, k, v, d_o, key_reach, blockmap, dk, dv, workspace, dev_status,
                        scale=None, stream=None):
+    _on_device(q=q, k=k, v=v, d_o=d_o, key_reach=key_reach, blockmap=blockmap, dk=dk, dv=dv,
+               workspace=workspace, dev_status=dev_status)
     T, Hq, d = q.shape
     scale = d ** -0.5 if scale is None else float(scale)
     _check("tree_attn_bwd_main", _lib.tree_attn_bwd_main(
@@ -318,6 +343,7 @@ def tree_attn_bwd_main(q, k, v, d_o, key_reach, blockmap, dk, dv, workspace, dev
 
 
 def tree_attn_bwd_finish(workspace, dq, dev_status, scale=None, stream=None):
+    _on_device(workspace=workspace, dq=dq, dev_status=dev_status)
     T, Hq, d = dq.shape
     scale = d ** -0.5 if scale is None else float(scale)
     _check("tree_attn_bwd_finish", _lib.tree_attn_bwd_finish(
@@ -332,6 +358,7 @@ def launch_count() -> int:
 
 def tree_debug_wait_timeout(dev_status, limit_ns: int, stream=None):
     """Run the bounded-wait probe; TREE_ERR_TIMEOUT lands in dev_status."""
+    _on_device(dev_status=dev_status)
     _check("tree_debug_wait_timeout", _lib.tree_debug_wait_timeout(
         _ptr(dev_status), int(limit_ns), _stream_ptr(stream)))
 

@@ -20,7 +20,10 @@ The same section names the companions: the entropy of the predictive
 distributions (``gather_packed_tree_logprobs_entropy``), vocabulary min/max
 statistics (``gather_packed_tree_vocab_stats``) and the merge of per-sequence
 results of several micro-batches back into a ``[batch, max_len]`` layout
-padded with ``padding_value`` (``merge_packed_tree_results``).
+padded with ``padding_value`` (``merge_packed_tree_results``), and a
+vocabulary-parallel mode (``tp_group``) in which each rank reduces a slice
+of the vocabulary; ``combine_vocab_slices`` restates the combination of the
+slices' row statistics.
 
 Readings where the page is silent:
 * the input is the packed logits ``[T_pad, V]`` (one row per packed token);
@@ -39,7 +42,8 @@ per-sequence computation with labels shifted by one, using scipy's
 log_softmax), by closed forms (uniform logits; one dominant logit), by brute
 force over small tries (the predecessor from parent pointers is the last
 visible key before the token in the dense ancestor mask), and by the cache
-count (every non-root-start token is a label exactly once).  See
+count (every non-root-start token is a label exactly once); the slice
+combination against scipy's logsumexp and entropy of the whole row.  See
 tests/test_oracle_logprob.py.
 """
 from __future__ import annotations
@@ -187,3 +191,31 @@ def packed_token_logprobs(logits, packed) -> np.ndarray:
         if pred[j] >= 0:
             out[j] = log_softmax(logits[pred[j]])[packed.token_ids[j]]
     return out
+
+
+def vocab_slices(V: int, n_slices: int) -> list[tuple[int, int]]:
+    """Contiguous vocabulary slices, as even as possible (the first V % n
+    slices one entry longer)."""
+    base, extra = divmod(V, n_slices)
+    out, a = [], 0
+    for r in range(n_slices):
+        b = a + base + (1 if r < extra else 0)
+        out.append((a, b))
+        a = b
+    return out
+
+
+def combine_vocab_slices(stats) -> tuple[float, float, float, float]:
+    """Row statistics of the whole vocabulary from those of its slices (the
+    page's vocabulary-parallel ``tp_group`` mode: each rank reduces its slice
+    of V).  ``stats`` holds each slice's (lse_r, entropy_r, min_r, max_r).
+    With w_r = exp(lse_r - lse) the share of slice r in the softmax mass:
+        lse     = log sum_r exp(lse_r)
+        entropy = sum_r w_r * (entropy_r + lse - lse_r)
+    (the entropy of the mixture of the slices' softmaxes with weights w_r)."""
+    lses = np.array([s[0] for s in stats], dtype=np.float64)
+    m = lses.max()
+    lse = m + np.log(np.exp(lses - m).sum())
+    w = np.exp(lses - lse)
+    ent = float((w * (np.array([s[1] for s in stats]) + lse - lses)).sum())
+    return float(lse), ent, float(min(s[2] for s in stats)), float(max(s[3] for s in stats))

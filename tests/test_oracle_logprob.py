@@ -200,3 +200,16 @@ def test_merge_across_micro_batches():
     capped = OL.merge_packed_tree_results(lp, 4, padding_value=0.0, max_len=2)
     assert capped.shape == (4, 2)
     np.testing.assert_allclose(capped[3], want[3][:2], atol=1e-12)
+
+
+@pytest.mark.parametrize("V,n", [(1000, 1), (1000, 2), (1001, 3), (151936, 8), (37, 5)])
+def test_vocab_parallel_combine_equals_whole_row(V, n):
+    x = _logits(1, V, V + n)[0]
+    x[3] += 12.0                      # one slice holds most of the mass
+    slices = OL.vocab_slices(V, n)
+    assert slices[0][0] == 0 and slices[-1][1] == V
+    assert all(b - a in (V // n, V // n + 1) for a, b in slices)
+    parts = [OL.row_stats(x[a:b]) for a, b in slices]
+    got = OL.combine_vocab_slices(parts)
+    want = (logsumexp(x), sp_entropy(softmax(x)), x.min(), x.max())
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)

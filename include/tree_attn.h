@@ -124,12 +124,18 @@ TREE_API tree_status_t tree_pack_positions(const int32_t* token_node, int32_t T_
  * workspace to pass.  The library keeps the scratch in one file-scope device
  * array of 1.75 MiB (held by every GPU that loads the library until the
  * process exits), enough for T_pad <= 65536 and n_nodes <= 65536; larger
- * sizes return TREE_ERR_WORKSPACE and launch nothing.  Nothing is allocated
- * or freed, by the library or by anything it calls.
+ * sizes return TREE_ERR_WORKSPACE and launch nothing.  The call makes no
+ * allocation call of any kind (no cudaMalloc, cudaFree or allocating library
+ * routine); the array itself is part of the library's CUDA module and is
+ * reserved on a device when that module is loaded there — under CUDA's lazy
+ * module loading, at the first call on that device.  A caller that needs the
+ * reservation made up front can make one call at start-up.
  *
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  Every call re-initialises the scratch it uses before reading it.
+ * device, with that device current) and remembers the CUDA context it found;
+ * make that first call before any stream capture.  A call that finds another
+ * context current (the primary context was reset and created again) looks
+ * the address up again.  Every call re-initialises the scratch it uses before reading it.
  * All calls share the one array, so calls whose work overlaps on the GPU
  * (other streams, other host threads) race and must be serialised.
  * Arguments, outputs and device-side errors are those of tree_pack_positions.
@@ -195,6 +201,8 @@ TREE_API tree_status_t tree_blockmap_build(const int32_t* key_reach, int32_t T_p
  *   q, k, v   [in]  device bf16 (layouts above)
  *   key_reach [in]  device int32[T_pad]
  *   blockmap  [in]  from tree_blockmap_build for the same key_reach
+ *   blockmap_bytes  size of the blockmap buffer; less than
+ *                   tree_blockmap_bytes(T_pad) is TREE_ERR_WORKSPACE
  *   d         [in]  64 or 128; Hq % Hkv == 0
  *   scale     [in]  softmax scale, positive and finite (1/sqrt(d) is the usual
  *                   choice); anything else is TREE_ERR_INVALID_ARG
@@ -203,9 +211,10 @@ TREE_API tree_status_t tree_blockmap_build(const int32_t* key_reach, int32_t T_p
  *   dev_status[out] TREE_ERR_TIMEOUT if a device wait ran out of time
  * ---------------------------------------------------------------------- */
 TREE_API tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v,
-                            const int32_t* key_reach, const void* blockmap, int32_t T_pad,
-                            int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o,
-                            float* lse, int32_t* dev_status, tree_stream_t stream);
+                            const int32_t* key_reach, const void* blockmap,
+                            size_t blockmap_bytes, int32_t T_pad, int32_t Hq, int32_t Hkv,
+                            int32_t d, float scale, void* o, float* lse, int32_t* dev_status,
+                            tree_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * tree_attn_bwd — backward of tree_attn_fwd.
@@ -221,6 +230,7 @@ TREE_API tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v
  * its dK/dV sum over all of them by construction.
  *
  *   o, d_o, lse   [in]  forward output, upstream gradient, forward LSE
+ *   blockmap, blockmap_bytes  as for tree_attn_fwd
  *   scale         [in]  the forward's scale (positive and finite)
  *   dq            [out] device bf16 [T_pad, Hq, d]
  *   dk, dv        [out] device bf16 [T_pad, Hkv, d]
@@ -230,10 +240,10 @@ TREE_API tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v
 TREE_API size_t tree_attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d);
 TREE_API tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                             const void* d_o, const float* lse, const int32_t* key_reach,
-                            const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
-                            int32_t d, float scale, void* dq, void* dk, void* dv,
-                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                            tree_stream_t stream);
+                            const void* blockmap, size_t blockmap_bytes, int32_t T_pad,
+                            int32_t Hq, int32_t Hkv, int32_t d, float scale, void* dq, void* dk,
+                            void* dv, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, tree_stream_t stream);
 
 /* The three steps of tree_attn_bwd, callable one by one on the same stream
  * (tree_attn_bwd is exactly prepare, main, finish):
@@ -251,10 +261,11 @@ TREE_API tree_status_t tree_attn_bwd_prepare(const void* o, const void* d_o, con
                                              int32_t* dev_status, tree_stream_t stream);
 TREE_API tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v,
                                           const void* d_o, const int32_t* key_reach,
-                                          const void* blockmap, int32_t T_pad, int32_t Hq,
-                                          int32_t Hkv, int32_t d, float scale, void* dk, void* dv,
-                                          void* workspace, size_t workspace_bytes,
-                                          int32_t* dev_status, tree_stream_t stream);
+                                          const void* blockmap, size_t blockmap_bytes,
+                                          int32_t T_pad, int32_t Hq, int32_t Hkv, int32_t d,
+                                          float scale, void* dk, void* dv, void* workspace,
+                                          size_t workspace_bytes, int32_t* dev_status,
+                                          tree_stream_t stream);
 TREE_API tree_status_t tree_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
                                             const void* workspace, size_t workspace_bytes,
                                             void* dq, int32_t* dev_status, tree_stream_t stream);

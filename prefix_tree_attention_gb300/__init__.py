@@ -39,11 +39,11 @@ _sig = {
     "tree_pack_positions": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P, _P]),
     "tree_blockmap_bytes": (_SZ, [_I32]),
     "tree_blockmap_build": (ctypes.c_int, [_P, _I32, _I32, _P, _SZ, _P, _P]),
-    "tree_attn_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32, _P, _P,
-                                     _P, _P]),
+    "tree_attn_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _SZ, _I32, _I32, _I32, _I32, _F32, _P,
+                                     _P, _P, _P]),
     "tree_attn_bwd_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
-    "tree_attn_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
-                                     _F32, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tree_attn_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I32, _I32, _I32,
+                                     _I32, _F32, _P, _P, _P, _P, _SZ, _P, _P]),
     "tree_packing_build": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _P]),
     "tree_packing_free": (None, [_P]),
     "tree_packing_num_tries": (_I32, [_P]),
@@ -52,8 +52,8 @@ _sig = {
     "tree_packing_seq_indices": (ctypes.c_int, [_P, _I32, _I32, _P, _I32]),
     "tree_debug_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
     "tree_attn_bwd_prepare": (ctypes.c_int, [_P, _P, _P, _I32, _I32, _I32, _P, _SZ, _P, _P]),
-    "tree_attn_bwd_main": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _F32,
-                                          _P, _P, _P, _SZ, _P, _P]),
+    "tree_attn_bwd_main": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _SZ, _I32, _I32, _I32, _I32,
+                                          _F32, _P, _P, _P, _SZ, _P, _P]),
     "tree_attn_bwd_finish": (ctypes.c_int, [_I32, _I32, _I32, _F32, _P, _SZ, _P, _P, _P]),
     "tree_launch_count": (ctypes.c_uint64, []),
     "tree_pack_positions_noalloc": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P, _P, _P]),
@@ -125,6 +125,17 @@ def _on_device(**tensors):
             raise ValueError(f"{name} must be a CUDA tensor")
 
 
+def _check_reach_blockmap(key_reach, blockmap, T):
+    """key_reach must hold T_pad int32 values; the blockmap buffer's size is
+    passed to the library, which refuses one that is too small."""
+    import torch
+    _need(key_reach, torch.int32, "key_reach")
+    if key_reach.numel() != T:
+        raise ValueError(f"key_reach must hold T_pad = {T} values, got {key_reach.numel()}")
+    if not blockmap.is_contiguous():
+        raise ValueError("blockmap must be contiguous")
+
+
 # --------------------------------------------------------------- workspaces
 def pack_positions_workspace_bytes(T_pad: int, n_nodes: int) -> int:
     return int(_lib.tree_pack_positions_workspace_bytes(T_pad, n_nodes))
@@ -193,10 +204,11 @@ def tree_attn_fwd(q, k, v, key_reach, blockmap, o, lse, dev_status, scale=None, 
     _need(lse, torch.float32, "lse")
     if k.shape != (T, Hkv, d) or v.shape != k.shape or o.shape != q.shape or lse.shape != (Hq, T):
         raise ValueError("shape mismatch")
+    _check_reach_blockmap(key_reach, blockmap, T)
     scale = d ** -0.5 if scale is None else float(scale)
     _check("tree_attn_fwd", _lib.tree_attn_fwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(key_reach), _ptr(blockmap), T, Hq, Hkv, d, scale,
-        _ptr(o), _ptr(lse), _ptr(dev_status), _stream_ptr(stream)))
+        _ptr(q), _ptr(k), _ptr(v), _ptr(key_reach), _ptr(blockmap), _nbytes(blockmap), T, Hq,
+        Hkv, d, scale, _ptr(o), _ptr(lse), _ptr(dev_status), _stream_ptr(stream)))
 
 
 def tree_attn_bwd(q, k, v, o, d_o, lse, key_reach, blockmap, dq, dk, dv, workspace, dev_status,
@@ -211,11 +223,15 @@ def tree_attn_bwd(q, k, v, o, d_o, lse, key_reach, blockmap, dq, dk, dv, workspa
         _need(t, torch.bfloat16, n)
     if dk.shape != k.shape or dv.shape != v.shape or dq.shape != q.shape or d_o.shape != q.shape:
         raise ValueError("shape mismatch")
+    if o.shape != q.shape or lse.shape != (Hq, T):
+        raise ValueError("shape mismatch")
+    _need(lse, torch.float32, "lse")
+    _check_reach_blockmap(key_reach, blockmap, T)
     scale = d ** -0.5 if scale is None else float(scale)
     _check("tree_attn_bwd", _lib.tree_attn_bwd(
         _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o), _ptr(lse), _ptr(key_reach),
-        _ptr(blockmap), T, Hq, Hkv, d, scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream_ptr(stream)))
+        _ptr(blockmap), _nbytes(blockmap), T, Hq, Hkv, d, scale, _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(workspace), _nbytes(workspace), _ptr(dev_status), _stream_ptr(stream)))
 
 
 def _nbytes(t) -> int:
@@ -335,11 +351,12 @@ def tree_attn_bwd_main(q, k, v, d_o, key_reach, blockmap, dk, dv, workspace, dev
     _on_device(q=q, k=k, v=v, d_o=d_o, key_reach=key_reach, blockmap=blockmap, dk=dk, dv=dv,
                workspace=workspace, dev_status=dev_status)
     T, Hq, d = q.shape
+    _check_reach_blockmap(key_reach, blockmap, T)
     scale = d ** -0.5 if scale is None else float(scale)
     _check("tree_attn_bwd_main", _lib.tree_attn_bwd_main(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(d_o), _ptr(key_reach), _ptr(blockmap), T, Hq,
-        k.shape[1], d, scale, _ptr(dk), _ptr(dv), _ptr(workspace), _nbytes(workspace),
-        _ptr(dev_status), _stream_ptr(stream)))
+        _ptr(q), _ptr(k), _ptr(v), _ptr(d_o), _ptr(key_reach), _ptr(blockmap),
+        _nbytes(blockmap), T, Hq, k.shape[1], d, scale, _ptr(dk), _ptr(dv), _ptr(workspace),
+        _nbytes(workspace), _ptr(dev_status), _stream_ptr(stream)))
 
 
 def tree_attn_bwd_finish(workspace, dq, dev_status, scale=None, stream=None):

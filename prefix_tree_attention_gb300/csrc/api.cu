@@ -178,9 +178,10 @@ tree_status_t tree_blockmap_build(const int32_t* key_reach, int32_t T_pad, int32
 }
 
 tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v,
-                            const int32_t* key_reach, const void* blockmap, int32_t T_pad,
-                            int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o,
-                            float* lse, int32_t* dev_status, tree_stream_t stream) {
+                            const int32_t* key_reach, const void* blockmap,
+                            size_t blockmap_bytes, int32_t T_pad, int32_t Hq, int32_t Hkv,
+                            int32_t d, float scale, void* o, float* lse, int32_t* dev_status,
+                            tree_stream_t stream) {
   tree_status_t st = check_attn_shape(T_pad, Hq, Hkv, d);
   if (st != TREE_OK) return st;
   if (!valid_scale(scale)) return TREE_ERR_INVALID_ARG;
@@ -190,6 +191,7 @@ tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(key_reach) || !aligned16(blockmap))
     return TREE_ERR_ALIGNMENT;
+  if (blockmap_bytes < tree_blockmap_bytes(T_pad)) return TREE_ERR_WORKSPACE;
   CUtensorMap tq, tk, tv;
   if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
       !encode_map(&tv, v, T_pad, Hkv, d))
@@ -220,10 +222,11 @@ tree_status_t tree_attn_bwd_prepare(const void* o, const void* d_o, const float*
 }
 
 tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v, const void* d_o,
-                                 const int32_t* key_reach, const void* blockmap, int32_t T_pad,
-                                 int32_t Hq, int32_t Hkv, int32_t d, float scale, void* dk,
-                                 void* dv, void* workspace, size_t workspace_bytes,
-                                 int32_t* dev_status, tree_stream_t stream) {
+                                 const int32_t* key_reach, const void* blockmap,
+                                 size_t blockmap_bytes, int32_t T_pad, int32_t Hq, int32_t Hkv,
+                                 int32_t d, float scale, void* dk, void* dv, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_status,
+                                 tree_stream_t stream) {
   tree_status_t st = check_attn_shape(T_pad, Hq, Hkv, d);
   if (st != TREE_OK) return st;
   if (!valid_scale(scale)) return TREE_ERR_INVALID_ARG;
@@ -235,6 +238,7 @@ tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v, co
   for (const void* p : ptrs)
     if (!aligned16(p)) return TREE_ERR_ALIGNMENT;
   if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
+  if (blockmap_bytes < tree_blockmap_bytes(T_pad)) return TREE_ERR_WORKSPACE;
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
       !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&tdo, d_o, T_pad, Hq, d) ||
@@ -263,10 +267,10 @@ tree_status_t tree_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float s
 
 tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v, const void* o,
                             const void* d_o, const float* lse, const int32_t* key_reach,
-                            const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
-                            int32_t d, float scale, void* dq, void* dk, void* dv,
-                            void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                            tree_stream_t stream) {
+                            const void* blockmap, size_t blockmap_bytes, int32_t T_pad,
+                            int32_t Hq, int32_t Hkv, int32_t d, float scale, void* dq, void* dk,
+                            void* dv, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, tree_stream_t stream) {
   tree_status_t st = check_attn_shape(T_pad, Hq, Hkv, d);
   if (st != TREE_OK) return st;
   if (!valid_scale(scale)) return TREE_ERR_INVALID_ARG;
@@ -275,11 +279,17 @@ tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v, const v
   if (!q || !k || !v || !o || !d_o || !lse || !key_reach || !blockmap || !dq || !dk || !dv ||
       !workspace)
     return TREE_ERR_INVALID_ARG;
+  // every argument error is returned before the first launch
+  const void* ptrs[] = {q, k, v, o, d_o, lse, key_reach, blockmap, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return TREE_ERR_ALIGNMENT;
+  if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
+  if (blockmap_bytes < tree_blockmap_bytes(T_pad)) return TREE_ERR_WORKSPACE;
   st = tree_attn_bwd_prepare(o, d_o, lse, T_pad, Hq, d, workspace, workspace_bytes, dev_status,
                              stream);
   if (st != TREE_OK) return st;
-  st = tree_attn_bwd_main(q, k, v, d_o, key_reach, blockmap, T_pad, Hq, Hkv, d, scale, dk, dv,
-                          workspace, workspace_bytes, dev_status, stream);
+  st = tree_attn_bwd_main(q, k, v, d_o, key_reach, blockmap, blockmap_bytes, T_pad, Hq, Hkv, d,
+                          scale, dk, dv, workspace, workspace_bytes, dev_status, stream);
   if (st != TREE_OK) return st;
   return tree_attn_bwd_finish(T_pad, Hq, d, scale, workspace, workspace_bytes, dq, dev_status,
                               stream);

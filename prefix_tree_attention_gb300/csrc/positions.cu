@@ -283,7 +283,11 @@ cudaError_t launch_pack_positions(const int32_t* token_node, int32_t T_pad,
 // cannot pass the array's name to a kernel (in host code it names a host-side
 // stand-in, not device memory), so the first call on each device looks up the
 // device address with cudaGetSymbolAddress, with that device current, and
-// caches it; make that first call before any stream capture.
+// caches it together with the CUDA context it belongs to; make that first
+// call before any stream capture.  A later call that finds a different
+// context current (the primary context was reset or torn down and created
+// again) looks the address up again, so no call ever launches with an
+// address from a context that no longer exists.
 namespace tree {
 namespace {
 
@@ -298,23 +302,54 @@ __device__ __align__(256) uint8_t g_positions_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchEntry {
+  void* ctx = nullptr;    // CUDA context the address was looked up in
+  void* addr = nullptr;   // device address of g_positions_scratch there
+};
+ScratchEntry g_scratch[kMaxDevices];
 
-// Device address of g_positions_scratch on the current device (looked up
-// once per device).
+// The driver's cuCtxGetCurrent, resolved once through the runtime (the
+// library does not link libcuda).
+using CtxGetCurrentFn = int (*)(void**);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Device address of g_positions_scratch on the current device, looked up
+// once per (device, context).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  CtxGetCurrentFn get_ctx = ctx_get_current();
+  if (!get_ctx) return cudaErrorDeviceUninitialized;
+  void* ctx = nullptr;
+  if (get_ctx(&ctx) != 0) return cudaErrorDeviceUninitialized;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchEntry& ent = g_scratch[dev];
+  // No context current yet on this thread (the runtime makes the primary
+  // context current lazily), or a different one: look the address up again.
+  // The lookup itself makes the device's primary context current.
+  if (!ent.addr || !ctx || ent.ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_positions_scratch);
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    if (get_ctx(&ctx) != 0 || !ctx) return cudaErrorDeviceUninitialized;
+    ent.ctx = ctx;
+    ent.addr = p;
   }
-  *out = g_scratch_addr[dev];
+  *out = ent.addr;
   return cudaSuccess;
 }
 

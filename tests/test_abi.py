@@ -57,10 +57,11 @@ def test_host_side_errors_return_before_launch():
     f = lib.tree_attn_fwd
     f.restype = ctypes.c_int
     P = ctypes.c_void_p
-    f.argtypes = [P, P, P, P, P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                  ctypes.c_int32, ctypes.c_float, P, P, P, P]
-    args = lambda T, Hq, Hkv, d, q=FAKE: (q, FAKE, FAKE, FAKE, FAKE, T, Hq, Hkv, d, 0.1,
-                                          FAKE, FAKE, FAKE, None)
+    f.argtypes = [P, P, P, P, P, ctypes.c_size_t, ctypes.c_int32, ctypes.c_int32,
+                  ctypes.c_int32, ctypes.c_int32, ctypes.c_float, P, P, P, P]
+    args = lambda T, Hq, Hkv, d, q=FAKE, bm_bytes=1 << 20: (
+        q, FAKE, FAKE, FAKE, FAKE, bm_bytes, T, Hq, Hkv, d, 0.1, FAKE, FAKE, FAKE, None)
+    assert f(*args(256, 4, 4, 64, bm_bytes=16)) == 8   # blockmap buffer too small
     assert f(*args(200, 4, 4, 64)) == 2          # T_pad not a multiple of 128
     assert f(*args(256, 4, 3, 64)) == 1          # Hq % Hkv
     assert f(*args(256, 4, 4, 96)) == 5          # head_dim unsupported
@@ -69,7 +70,7 @@ def test_host_side_errors_return_before_launch():
     assert f(*args(0, 4, 4, 64)) == 0            # empty input is a no-op
     for bad in (0.0, -0.1, float("nan"), float("inf")):   # scale not positive and finite
         a = list(args(256, 4, 4, 64))
-        a[9] = bad
+        a[10] = bad
         assert f(*a) == 1, bad
     b = lib.tree_blockmap_build
     b.restype = ctypes.c_int
@@ -85,10 +86,14 @@ def test_host_side_errors_return_before_launch():
     assert pp(FAKE, 100, FAKE, FAKE, 4, FAKE, FAKE, FAKE, 1 << 20, FAKE, None) == 2
     bw = lib.tree_attn_bwd
     bw.restype = ctypes.c_int
-    bw.argtypes = [P] * 8 + [ctypes.c_int32] * 4 + [ctypes.c_float] + [P] * 4 + \
-        [ctypes.c_size_t, P, P]
-    assert bw(*([FAKE] * 8), 256, 8, 2, 128, 0.1, FAKE, FAKE, FAKE, FAKE, 64, FAKE, None) == 8
-    assert bw(*([FAKE] * 8), 256, 8, 2, 128, -1.0, FAKE, FAKE, FAKE, FAKE, 1 << 30, FAKE,
+    bw.argtypes = [P] * 8 + [ctypes.c_size_t] + [ctypes.c_int32] * 4 + [ctypes.c_float] + \
+        [P] * 4 + [ctypes.c_size_t, P, P]
+    MB = 1 << 20
+    assert bw(*([FAKE] * 8), MB, 256, 8, 2, 128, 0.1, FAKE, FAKE, FAKE, FAKE, 64, FAKE,
+              None) == 8                                     # workspace too small
+    assert bw(*([FAKE] * 8), 16, 256, 8, 2, 128, 0.1, FAKE, FAKE, FAKE, FAKE, 1 << 30, FAKE,
+              None) == 8                                     # blockmap too small
+    assert bw(*([FAKE] * 8), MB, 256, 8, 2, 128, -1.0, FAKE, FAKE, FAKE, FAKE, 1 << 30, FAKE,
               None) == 1
 
 

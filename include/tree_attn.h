@@ -487,6 +487,52 @@ TREE_API tree_status_t tree_dta_schedule(const int32_t* token_node, int32_t T_pa
                                          int64_t* peak_stack_tokens);
 
 /* ------------------------------------------------------------------------
+ * tree_dta_attn — attention forward and backward executed through the
+ * depth-first traversal of dynamic tree attention.
+ *
+ * Source: AREAL-DTA, sections 3.1 (forward and push on the way down, a
+ * leaf's backward as soon as its sequence is complete, a node's backward when
+ * it is popped, after all its descendants) and 3.2 (chunked backward, no leaf
+ * KV caching).  On the packed layout every key/value row stays resident, so
+ * the stack is implicit: at each operation it holds exactly the ancestor
+ * tokens of the operation's rows, which are the keys the packed mask lets
+ * them see.  Each operation is therefore the packed tree attention
+ * restricted to its query rows [t0, t1):
+ *   TREE_DTA_FWD_PUSH  forward of the rows (O, LSE of those rows)
+ *   TREE_DTA_FWD_BWD   forward, then backward of the rows
+ *   TREE_DTA_BWD_POP   backward of the rows
+ * A backward writes dQ of its rows and adds its rows' contributions to dK and
+ * dV of every key they see into fp32 accumulators (a shared-prefix key thus
+ * sums every continuation's rows, in traversal order); after the last
+ * operation dK and dV are rounded to bf16.  O, dQ start at 0 and LSE at
+ * -inf, so rows no operation covers (pads) keep those values and get zero
+ * key gradients.  With a schedule from tree_dta_schedule (every real row in
+ * one forward and one backward, forward first) the results equal
+ * tree_attn_fwd + tree_attn_bwd up to fp32 summation order.
+ *
+ *   q, k, v, d_o, key_reach, blockmap, blockmap_bytes, T_pad, Hq, Hkv, d,
+ *   scale          as for tree_attn_fwd / tree_attn_bwd
+ *   ops            [in]  HOST int32[n_ops][3] of (kind, t0, t1), executed in
+ *                        order; kind in {0,1,2}, 0 <= t0 < t1 <= T_pad, else
+ *                        TREE_ERR_INVALID_ARG before any launch
+ *   o, lse         [out] forward outputs (layouts as for tree_attn_fwd)
+ *   dq, dk, dv     [out] gradients (layouts as for tree_attn_bwd)
+ *   workspace      [tmp] >= tree_dta_attn_workspace_bytes(T_pad, Hq, Hkv, d):
+ *                        the tree_attn_bwd workspace followed by fp32 dK and
+ *                        dV accumulators [T_pad, Hkv, d]
+ * Launches: 2 + one per FWD_PUSH, four per FWD_BWD, three per BWD_POP, all
+ * queued on `stream` with no host synchronisation.
+ * ---------------------------------------------------------------------- */
+TREE_API size_t tree_dta_attn_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t Hkv, int32_t d);
+TREE_API tree_status_t tree_dta_attn(const void* q, const void* k, const void* v, const void* d_o,
+                                     const int32_t* key_reach, const void* blockmap,
+                                     size_t blockmap_bytes, int32_t T_pad, int32_t Hq,
+                                     int32_t Hkv, int32_t d, float scale, const int32_t* ops,
+                                     int64_t n_ops, void* o, float* lse, void* dq, void* dk,
+                                     void* dv, void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_status, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  *
  * tree_debug_wait_timeout — launch one warp that waits on a shared-memory

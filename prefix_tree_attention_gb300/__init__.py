@@ -63,6 +63,9 @@ _sig = {
     "tree_merge_per_sequence": (ctypes.c_int, [_P, _I64, _P, _I64, _P, _I32, _I32, _I32, _I32,
                                                _F32, _P, _P, _P]),
     "tree_dta_schedule": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _P]),
+    "tree_dta_attn_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32]),
+    "tree_dta_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _SZ, _I32, _I32, _I32, _I32, _F32,
+                                     _P, _I64, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
 }
 for _name, (_res, _args) in _sig.items():
     _fn = getattr(_lib, _name)
@@ -318,6 +321,39 @@ def dta_schedule(token_node, node_entry, node_exit, chunk: int = 2048):
     _check("tree_dta_schedule", _lib.tree_dta_schedule(*args, ops.ctypes.data, n_ops.value,
                                                        ctypes.byref(n_ops), ctypes.byref(peak)))
     return ops[:n_ops.value], int(peak.value)
+
+
+def dta_attn_workspace_bytes(T_pad: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(_lib.tree_dta_attn_workspace_bytes(T_pad, Hq, Hkv, d))
+
+
+def tree_dta_attn(q, k, v, d_o, key_reach, blockmap, ops, o, lse, dq, dk, dv, workspace,
+                  dev_status, scale=None, stream=None):
+    """Attention forward + backward executed op by op through a depth-first
+    traversal schedule ``ops`` (host int32 ``[n_ops, 3]`` of (kind, t0, t1),
+    e.g. from :func:`dta_schedule`)."""
+    import torch
+    _on_device(q=q, k=k, v=v, d_o=d_o, key_reach=key_reach, blockmap=blockmap, o=o, lse=lse,
+               dq=dq, dk=dk, dv=dv, workspace=workspace, dev_status=dev_status)
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (d_o, "d_o"), (o, "o"), (dq, "dq"), (dk, "dk"),
+                 (dv, "dv")):
+        _need(t, torch.bfloat16, n)
+    _need(lse, torch.float32, "lse")
+    if (k.shape != (T, Hkv, d) or v.shape != k.shape or d_o.shape != q.shape or
+            o.shape != q.shape or dq.shape != q.shape or dk.shape != k.shape or
+            dv.shape != k.shape or lse.shape != (Hq, T)):
+        raise ValueError("shape mismatch")
+    _check_reach_blockmap(key_reach, blockmap, T)
+    host_ops = np.ascontiguousarray(ops, dtype=np.int32).reshape(-1, 3)
+    scale = d ** -0.5 if scale is None else float(scale)
+    _check("tree_dta_attn", _lib.tree_dta_attn(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(d_o), _ptr(key_reach), _ptr(blockmap),
+        _nbytes(blockmap), T, Hq, Hkv, d, scale,
+        host_ops.ctypes.data if host_ops.size else None, host_ops.shape[0], _ptr(o), _ptr(lse),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), _nbytes(workspace), _ptr(dev_status),
+        _stream_ptr(stream)))
 
 
 def sequence_index_arrays(tries, n_seqs: int, trie_offsets=None):

@@ -22,7 +22,7 @@ LIB_NAME = "libtreeattn.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 CUDA_SOURCES = ["api.cu", "positions.cu", "blockmap.cu", "attn_fwd.cu", "attn_bwd.cu",
-                "diag.cu", "logprob.cu"]
+                "diag.cu", "logprob.cu", "dta_attn.cu"]
 CXX_SOURCES = ["packer.cpp", "partition.cpp", "dta.cpp"]
 
 

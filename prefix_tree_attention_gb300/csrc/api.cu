@@ -15,20 +15,28 @@ namespace tree {
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const int32_t* key_reach, const void* blockmap, int32_t T_pad,
                             int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o, float* lse,
-                            int32_t* status, cudaStream_t s);
+                            int32_t* status, cudaStream_t s, int32_t row_lo, int32_t row_hi);
 size_t attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d);
 cudaError_t launch_attn_bwd_prepare(const void* o, const void* d_o, const float* lse,
                                     int32_t T_pad, int32_t Hq, int32_t d, void* workspace,
-                                    int32_t* status, cudaStream_t s, int num_sms);
+                                    int32_t* status, cudaStream_t s, int num_sms, int32_t row_lo,
+                                    int32_t row_hi);
 cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo,
                                  const CUtensorMap& tdq, const int32_t* key_reach,
                                  const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
                                  int32_t d, float scale, void* dk, void* dv, void* workspace,
-                                 int32_t* status, cudaStream_t s, int num_sms);
+                                 int32_t* status, cudaStream_t s, int num_sms, int32_t row_lo,
+                                 int32_t row_hi, float* dk_acc, float* dv_acc);
 cudaError_t launch_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
                                    void* workspace, void* dq, int32_t* status, cudaStream_t s,
-                                   int num_sms);
+                                   int num_sms, int32_t row_lo, int32_t row_hi);
+cudaError_t launch_dta_init(void* o, void* dq, float* lse, void* workspace, size_t ws_bytes,
+                            int32_t T_pad, int32_t Hq, int32_t d, int32_t* status,
+                            cudaStream_t s, int num_sms);
+cudaError_t launch_dta_finish(const float* dk_acc, const float* dv_acc, void* dk, void* dv,
+                              int32_t T_pad, int32_t Hkv, int32_t d, int32_t* status,
+                              cudaStream_t s, int num_sms);
 
 namespace {
 std::atomic<uint64_t> g_launches{0};
@@ -197,7 +205,7 @@ tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v,
       !encode_map(&tv, v, T_pad, Hkv, d))
     return TREE_ERR_CUDA;
   return cuda_result(tree::launch_attn_fwd(tq, tk, tv, key_reach, blockmap, T_pad, Hq, Hkv, d,
-                                           scale, o, lse, dev_status, stream));
+                                           scale, o, lse, dev_status, stream, 0, T_pad));
 }
 
 size_t tree_attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d) {
@@ -218,7 +226,8 @@ tree_status_t tree_attn_bwd_prepare(const void* o, const void* d_o, const float*
     return TREE_ERR_ALIGNMENT;
   if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
   return cuda_result(tree::launch_attn_bwd_prepare(o, d_o, lse, T_pad, Hq, d, workspace,
-                                                   dev_status, stream, num_sms_current()));
+                                                   dev_status, stream, num_sms_current(), 0,
+                                                   T_pad));
 }
 
 tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v, const void* d_o,
@@ -246,7 +255,8 @@ tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v, co
     return TREE_ERR_CUDA;
   return cuda_result(tree::launch_attn_bwd_main(tq, tk, tv, tdo, tdq, key_reach, blockmap, T_pad,
                                                 Hq, Hkv, d, scale, dk, dv, workspace, dev_status,
-                                                stream, num_sms_current()));
+                                                stream, num_sms_current(), 0, T_pad, nullptr,
+                                                nullptr));
 }
 
 tree_status_t tree_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
@@ -262,7 +272,7 @@ tree_status_t tree_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float s
   if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
   return cuda_result(tree::launch_attn_bwd_finish(T_pad, Hq, d, scale,
                                                   const_cast<void*>(workspace), dq, dev_status,
-                                                  stream, num_sms_current()));
+                                                  stream, num_sms_current(), 0, T_pad));
 }
 
 tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -293,6 +303,72 @@ tree_status_t tree_attn_bwd(const void* q, const void* k, const void* v, const v
   if (st != TREE_OK) return st;
   return tree_attn_bwd_finish(T_pad, Hq, d, scale, workspace, workspace_bytes, dq, dev_status,
                               stream);
+}
+
+size_t tree_dta_attn_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t Hkv, int32_t d) {
+  if (T_pad < 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return 0;
+  return tree::attn_bwd_workspace_bytes(T_pad, Hq, d) +
+         2 * static_cast<size_t>(T_pad) * Hkv * d * sizeof(float);
+}
+
+tree_status_t tree_dta_attn(const void* q, const void* k, const void* v, const void* d_o,
+                            const int32_t* key_reach, const void* blockmap,
+                            size_t blockmap_bytes, int32_t T_pad, int32_t Hq, int32_t Hkv,
+                            int32_t d, float scale, const int32_t* ops, int64_t n_ops, void* o,
+                            float* lse, void* dq, void* dk, void* dv, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, tree_stream_t stream) {
+  tree_status_t st = check_attn_shape(T_pad, Hq, Hkv, d);
+  if (st != TREE_OK) return st;
+  if (!valid_scale(scale) || !dev_status || n_ops < 0) return TREE_ERR_INVALID_ARG;
+  if (T_pad == 0) return TREE_OK;
+  if (!q || !k || !v || !d_o || !key_reach || !blockmap || !o || !lse || !dq || !dk || !dv ||
+      !workspace || (n_ops > 0 && !ops))
+    return TREE_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, d_o, key_reach, blockmap, o, lse, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return TREE_ERR_ALIGNMENT;
+  if (workspace_bytes < tree_dta_attn_workspace_bytes(T_pad, Hq, Hkv, d))
+    return TREE_ERR_WORKSPACE;
+  if (blockmap_bytes < tree_blockmap_bytes(T_pad)) return TREE_ERR_WORKSPACE;
+  for (int64_t i = 0; i < n_ops; ++i) {
+    const int32_t kind = ops[3 * i], t0 = ops[3 * i + 1], t1 = ops[3 * i + 2];
+    if (kind < TREE_DTA_FWD_PUSH || kind > TREE_DTA_BWD_POP || t0 < 0 || t1 <= t0 || t1 > T_pad)
+      return TREE_ERR_INVALID_ARG;
+  }
+  // the bwd workspace (dQ accumulator, D and LSE rows) leads; the fp32 dK and
+  // dV accumulators follow
+  const size_t bwd_bytes = tree::attn_bwd_workspace_bytes(T_pad, Hq, d);
+  float* dk_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_bytes);
+  float* dv_acc = dk_acc + static_cast<size_t>(T_pad) * Hkv * d;
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
+      !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&tdo, d_o, T_pad, Hq, d) ||
+      !encode_map_acc(&tdq, workspace, T_pad, Hq, d))
+    return TREE_ERR_CUDA;
+  const int sms = num_sms_current();
+  cudaError_t e = tree::launch_dta_init(o, dq, lse, workspace,
+                                        tree_dta_attn_workspace_bytes(T_pad, Hq, Hkv, d), T_pad,
+                                        Hq, d, dev_status, stream, sms);
+  for (int64_t i = 0; e == cudaSuccess && i < n_ops; ++i) {
+    const int32_t kind = ops[3 * i], t0 = ops[3 * i + 1], t1 = ops[3 * i + 2];
+    if (kind != TREE_DTA_BWD_POP)     // forward of the rows against their visible keys
+      e = tree::launch_attn_fwd(tq, tk, tv, key_reach, blockmap, T_pad, Hq, Hkv, d, scale, o,
+                                lse, dev_status, stream, t0, t1);
+    if (e == cudaSuccess && kind != TREE_DTA_FWD_PUSH) {   // backward of the rows
+      e = tree::launch_attn_bwd_prepare(o, d_o, lse, T_pad, Hq, d, workspace, dev_status,
+                                        stream, sms, t0, t1);
+      if (e == cudaSuccess)
+        e = tree::launch_attn_bwd_main(tq, tk, tv, tdo, tdq, key_reach, blockmap, T_pad, Hq,
+                                       Hkv, d, scale, dk, dv, workspace, dev_status, stream,
+                                       sms, t0, t1, dk_acc, dv_acc);
+      if (e == cudaSuccess)
+        e = tree::launch_attn_bwd_finish(T_pad, Hq, d, scale, workspace, dq, dev_status, stream,
+                                         sms, t0, t1);
+    }
+  }
+  if (e == cudaSuccess)
+    e = tree::launch_dta_finish(dk_acc, dv_acc, dk, dv, T_pad, Hkv, d, dev_status, stream, sms);
+  return cuda_result(e);
 }
 
 uint64_t tree_launch_count(void) { return tree::launches_total(); }

@@ -80,7 +80,16 @@ struct BwdParams {
   float* dq_acc;              // [T_pad, Hq, D]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
+  // Accumulate mode (both non-null): dK (scaled) and dV are added in fp32
+  // into these [T_pad, Hkv, D] rows instead of being stored as bf16, and a
+  // key block whose clipped column run is empty leaves its rows untouched.
+  float* dk_acc;
+  float* dv_acc;
   int32_t T_pad, Hq, Hkv, nb, num_sms;
+  // Query-row window [row_lo, row_hi): only these rows' gradients flow; each
+  // key block's column run is clipped to the query blocks the window meets,
+  // and rows outside it count as masked.
+  int32_t row_lo, row_hi, windowed;
   float scale, scale_log2;
   int32_t* status;
 };
@@ -153,15 +162,8 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&sm.drain, 1);
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
-    tmem_alloc(&sm.tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   int32_t heavy_n = __syncthreads_count(heavy_local > 0);
   for (int i = 1; i * kBwdThreads < p.nb; ++i) heavy_n += __syncthreads_count(heavy_local > i);
-  tc_fence_after();
-  const uint32_t tbase = sm.tmem_slot;
   int32_t kvh, rank;
   if (static_cast<int32_t>(blockIdx.x) < heavy_n * p.Hkv) {
     kvh = blockIdx.x / heavy_n;
@@ -172,10 +174,22 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     rank = heavy_n + j % nl;
   }
   const int32_t kb = bm.col_order()[rank];
-  const int32_t col_hi = bm.col_hi()[kb];
   const int32_t col_full_hi = bm.col_full_hi()[kb];
-  const int32_t col_len = col_hi >= kb ? col_hi - kb + 1 : 0;
+  // the key block's column run kb..col_hi, clipped to the window's blocks
+  const int32_t qa_first = max(kb, p.row_lo / kBlock);
+  const int32_t qa_last = min(bm.col_hi()[kb], (p.row_hi - 1) / kBlock);
+  const int32_t col_len = qa_last >= qa_first ? qa_last - qa_first + 1 : 0;
   const int32_t nsteps = col_len * g;
+  const bool accumulate = p.dk_acc != nullptr;
+  if (accumulate && nsteps == 0) return;     // CTA-uniform: nothing to add
+  if (warp == kWarpMma) {
+    tmem_alloc(&sm.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_slot;
   constexpr uint32_t kTileBytes = kBlock * D * 2;
   constexpr int kHalves = D / 64;
   constexpr uint32_t kDV = 0, kDK = 128, kS = 256, kDP = 384, kDQ = 384;
@@ -196,7 +210,7 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         const int s = n & 1;
         if (n >= 2 && !mbar_wait(&sm.empty[s], ((n >> 1) - 1) & 1, ab)) break;
         const int32_t h = kvh * g + n % g;      // query block outer, heads inner
-        const int32_t qa = kb + n / g;
+        const int32_t qa = qa_first + n / g;
         mbar_arrive_expect_tx(&sm.full[s], 2 * kTileBytes + 2 * kBlock * 4);
         for (int hf = 0; hf < kHalves; ++hf) {
           tma_load_3d(sm.q[s] + hf * kBlock * 64, &tm_q, &sm.full[s], hf * 64, h, qa * kBlock);
@@ -292,7 +306,7 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool ok = true;
     for (int n = 0; ok && n < nsteps; ++n) {
       const int32_t h = kvh * g + n % g;
-      const int32_t qa = kb + n / g;
+      const int32_t qa = qa_first + n / g;
       const int row0 = qa * kBlock + quarter * 32;
       if (!(ok = mbar_wait_warp(&sm.dq_full, n & 1, ab))) break;
       tc_fence_after();
@@ -339,8 +353,10 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool ok = true;
     for (int n = 0; ok && n < nsteps; ++n) {
       const int s = n & 1;
-      const int32_t qa = kb + n / g;
-      const bool partial = (qa == kb) || (qa > col_full_hi);
+      const int32_t qa = qa_first + n / g;
+      // window edges count as PARTIAL: rows outside the window are masked
+      const bool partial = (qa == kb) || (qa > col_full_hi) ||
+                           (p.windowed && (qa * kBlock < p.row_lo || qa * kBlock + kBlock > p.row_hi));
       if (!(ok = mbar_wait_warp(&sm.s_full, n & 1, ab))) break;
       tc_fence_after();
       float pv[64];
@@ -370,9 +386,10 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
       if (partial) {   // warp-uniform: only PARTIAL tiles evaluate the mask
         const int32_t q0 = qa * kBlock + w * 64;
+        const int32_t lo = max(jkey, p.row_lo), hi = min(reach, p.row_hi - 1);
 #pragma unroll
         for (int c = 0; c < 64; ++c)
-          if (!(jkey <= q0 + c && q0 + c <= reach)) pv[c] = 0.f;
+          if (!(lo <= q0 + c && q0 + c <= hi)) pv[c] = 0.f;
       }
       if (!(ok = mbar_wait_warp(&sm.dp_full, n & 1, ab))) break;
       tc_fence_after();
@@ -421,9 +438,40 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_arrive(&sm.ew_done);
     }
     // ---------------------------------------------------------- epilogue
-    __nv_bfloat16* dvrow = p.dv + (static_cast<size_t>(jkey) * p.Hkv + kvh) * D + w * (D / 2);
-    __nv_bfloat16* dkrow = p.dk + (static_cast<size_t>(jkey) * p.Hkv + kvh) * D + w * (D / 2);
-    if (ok && nsteps > 0 && mbar_wait_warp(&sm.dvdk_done, (nsteps - 1) & 1, ab)) {
+    const size_t row_off = (static_cast<size_t>(jkey) * p.Hkv + kvh) * D + w * (D / 2);
+    __nv_bfloat16* dvrow = p.dv + row_off;
+    __nv_bfloat16* dkrow = p.dk + row_off;
+    if (accumulate) {
+      // fp32 read-add-write of this key row's half: within one launch each
+      // (key, kv head) row belongs to exactly one CTA, so no atomics
+      if (ok && mbar_wait_warp(&sm.dvdk_done, (nsteps - 1) & 1, ab)) {
+        tc_fence_after();
+        float* av = p.dv_acc + row_off;
+        float* ak = p.dk_acc + row_off;
+#pragma unroll
+        for (int c2 = 0; c2 < D / 64; ++c2) {
+          uint32_t rv[32], rk[32];
+          tmem_ld32x2(tbase + lane_off + kDV + w * (D / 2) + c2 * 32,
+                      tbase + lane_off + kDK + w * (D / 2) + c2 * 32, rv, rk);
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            float4* pv4 = reinterpret_cast<float4*>(av + c2 * 32 + e4 * 4);
+            float4* pk4 = reinterpret_cast<float4*>(ak + c2 * 32 + e4 * 4);
+            float4 a = *pv4, b = *pk4;
+            a.x += __uint_as_float(rv[4 * e4]);
+            a.y += __uint_as_float(rv[4 * e4 + 1]);
+            a.z += __uint_as_float(rv[4 * e4 + 2]);
+            a.w += __uint_as_float(rv[4 * e4 + 3]);
+            b.x += __uint_as_float(rk[4 * e4]) * p.scale;
+            b.y += __uint_as_float(rk[4 * e4 + 1]) * p.scale;
+            b.z += __uint_as_float(rk[4 * e4 + 2]) * p.scale;
+            b.w += __uint_as_float(rk[4 * e4 + 3]) * p.scale;
+            *pv4 = a;
+            *pk4 = b;
+          }
+        }
+      }
+    } else if (ok && nsteps > 0 && mbar_wait_warp(&sm.dvdk_done, (nsteps - 1) & 1, ab)) {
       tc_fence_after();
 #pragma unroll
       for (int c2 = 0; c2 < D / 64; ++c2) {
@@ -467,12 +515,14 @@ template <int D>
 __global__ void __launch_bounds__(256)
 tree_attn_bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse,
                           float* dd, float* lse2, float* dq_acc, int32_t T_pad, int32_t Hq,
-                          const int32_t* status) {
+                          int32_t row_lo, int32_t row_hi, const int32_t* status) {
   if (ld_status(status)) return;
-  const int64_t rows = static_cast<int64_t>(T_pad) * Hq;
+  // (token, head) rows of the token window [row_lo, row_hi)
+  const int64_t rows = static_cast<int64_t>(row_hi) * Hq;
   const int lane = threadIdx.x & 31;
-  for (int64_t row = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; row < rows;
-       row += (int64_t(gridDim.x) * blockDim.x) >> 5) {
+  for (int64_t row = static_cast<int64_t>(row_lo) * Hq +
+                     ((blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5);
+       row < rows; row += (int64_t(gridDim.x) * blockDim.x) >> 5) {
     const int64_t i = row / Hq, h = row % Hq;
     constexpr int kPer = D / 32;     // elements per lane (2 or 4)
     float acc = 0.f;
@@ -498,10 +548,10 @@ tree_attn_bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, con
 
 // a6: dQ = bf16(scale * acc), 8 elements per thread.
 __global__ void __launch_bounds__(256)
-tree_attn_bwd_dq_kernel(const float* dq_acc, __nv_bfloat16* dq, int64_t n8, float scale,
-                        const int32_t* status) {
+tree_attn_bwd_dq_kernel(const float* dq_acc, __nv_bfloat16* dq, int64_t t_lo, int64_t t_hi,
+                        float scale, const int32_t* status) {
   if (ld_status(status)) return;
-  for (int64_t t = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; t < n8;
+  for (int64_t t = t_lo + blockIdx.x * int64_t(blockDim.x) + threadIdx.x; t < t_hi;
        t += int64_t(gridDim.x) * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * t];
     const float4 b = reinterpret_cast<const float4*>(dq_acc)[2 * t + 1];
@@ -540,18 +590,20 @@ size_t attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d) {
 
 cudaError_t launch_attn_bwd_prepare(const void* o, const void* d_o, const float* lse,
                                     int32_t T_pad, int32_t Hq, int32_t d, void* workspace,
-                                    int32_t* status, cudaStream_t s, int num_sms) {
+                                    int32_t* status, cudaStream_t s, int num_sms,
+                                    int32_t row_lo, int32_t row_hi) {
   BwdWorkspace w = carve(workspace, T_pad, Hq, d);
-  const int64_t rows = static_cast<int64_t>(T_pad) * Hq;
+  if (row_hi <= row_lo) return cudaSuccess;
+  const int64_t rows = static_cast<int64_t>(row_hi - row_lo) * Hq;
   const int blocks = grid_cap((rows * 32 + 255) / 256, num_sms);
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(d_o);
   if (d == 64)
     tree_attn_bwd_prep_kernel<64><<<blocks, 256, 0, s>>>(po, pd, lse, w.dd, w.lse2, w.dq_acc,
-                                                         T_pad, Hq, status);
+                                                         T_pad, Hq, row_lo, row_hi, status);
   else
     tree_attn_bwd_prep_kernel<128><<<blocks, 256, 0, s>>>(po, pd, lse, w.dd, w.lse2, w.dq_acc,
-                                                          T_pad, Hq, status);
+                                                          T_pad, Hq, row_lo, row_hi, status);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -561,8 +613,10 @@ cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tdq, const int32_t* key_reach,
                                  const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
                                  int32_t d, float scale, void* dk, void* dv, void* workspace,
-                                 int32_t* status, cudaStream_t s, int num_sms) {
+                                 int32_t* status, cudaStream_t s, int num_sms, int32_t row_lo,
+                                 int32_t row_hi, float* dk_acc, float* dv_acc) {
   BwdWorkspace w = carve(workspace, T_pad, Hq, d);
+  if (row_hi <= row_lo) return cudaSuccess;
   BwdParams p;
   p.key_reach = key_reach;
   p.blockmap = static_cast<const int32_t*>(blockmap);
@@ -571,6 +625,11 @@ cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
   p.dq_acc = w.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.dk_acc = dk_acc;
+  p.dv_acc = dv_acc;
+  p.row_lo = row_lo;
+  p.row_hi = row_hi;
+  p.windowed = (row_lo > 0 || row_hi < T_pad) ? 1 : 0;
   p.T_pad = T_pad;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -602,11 +661,14 @@ cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
 
 cudaError_t launch_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
                                    void* workspace, void* dq, int32_t* status, cudaStream_t s,
-                                   int num_sms) {
+                                   int num_sms, int32_t row_lo, int32_t row_hi) {
   BwdWorkspace w = carve(workspace, T_pad, Hq, d);
-  const int64_t n8 = static_cast<int64_t>(T_pad) * Hq * d / 8;
-  tree_attn_bwd_dq_kernel<<<grid_cap((n8 + 255) / 256, num_sms), 256, 0, s>>>(
-      w.dq_acc, static_cast<__nv_bfloat16*>(dq), n8, scale, status);
+  if (row_hi <= row_lo) return cudaSuccess;
+  // groups of 8 elements; a token row holds Hq * d (a multiple of 64) of them
+  const int64_t per_row8 = static_cast<int64_t>(Hq) * d / 8;
+  const int64_t t_lo = row_lo * per_row8, t_hi = row_hi * per_row8;
+  tree_attn_bwd_dq_kernel<<<grid_cap((t_hi - t_lo + 255) / 256, num_sms), 256, 0, s>>>(
+      w.dq_acc, static_cast<__nv_bfloat16*>(dq), t_lo, t_hi, scale, status);
   count_launches(1);
   return cudaGetLastError();
 }

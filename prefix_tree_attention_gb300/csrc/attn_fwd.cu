@@ -55,6 +55,10 @@ struct FwdParams {
   const int32_t* key_reach;
   const int32_t* blockmap;
   int32_t T_pad, Hq, Hkv, nb, heads_per_cta, n_hgroups;
+  // Query-row window [row_lo, row_hi): only these rows' O and LSE are
+  // written.  The grid covers query blocks qa_lo .. qa_lo + n_qa - 1; with
+  // the whole trie as the window they are visited heaviest row first.
+  int32_t row_lo, row_hi, qa_lo, n_qa, windowed;
   float scale_log2;                    // softmax scale * log2(e)
   __nv_bfloat16* o;
   float* lse;
@@ -277,9 +281,9 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   // first, so the last kv head's long rows start with twice the span of a
   // single head group ahead of them.
   const int32_t gpk = p.n_hgroups / p.Hkv;          // head groups per kv head
-  const int32_t unit = blockIdx.x / (gpk * p.nb);
-  const int32_t j = blockIdx.x % (gpk * p.nb);
-  const int32_t qa = bm.row_order()[j / gpk];
+  const int32_t unit = blockIdx.x / (gpk * p.n_qa);
+  const int32_t j = blockIdx.x % (gpk * p.n_qa);
+  const int32_t qa = p.windowed ? p.qa_lo + j / gpk : bm.row_order()[j / gpk];
   const int32_t h0 = (unit * gpk + j % gpk) * p.heads_per_cta;
   const int nh = p.heads_per_cta;
   const int32_t kvh = h0 / (p.Hq / p.Hkv);
@@ -426,6 +430,9 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         mbar_arrive(&sm.p_full[t]);
       }
       // ---------------------------------------------------------- epilogue
+      // (every lane takes part in the warp-collective TMEM loads; only rows
+      // inside the window store)
+      const bool in_window = i >= p.row_lo && i < p.row_hi;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(i) * p.Hq + h) * D;
       if (ok && ntiles > 0 && mbar_wait_warp(&sm.o_full[t], (ntiles - 1) & 1, ab)) {
         tc_fence_after();
@@ -441,12 +448,13 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             w.y = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 2]) * inv_l, __uint_as_float(reg[e8 * 8 + 3]) * inv_l);
             w.z = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 4]) * inv_l, __uint_as_float(reg[e8 * 8 + 5]) * inv_l);
             w.w = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 6]) * inv_l, __uint_as_float(reg[e8 * 8 + 7]) * inv_l);
-            *reinterpret_cast<uint4*>(orow + c4 * 32 + e8 * 8) = w;
+            if (in_window) *reinterpret_cast<uint4*>(orow + c4 * 32 + e8 * 8) = w;
           }
         }
-        p.lse[static_cast<size_t>(h) * p.T_pad + i] =
-            l > 0.f ? m * 0.69314718055994531f + logf(l) : -INFINITY;
-      } else if (ntiles == 0) {
+        if (in_window)
+          p.lse[static_cast<size_t>(h) * p.T_pad + i] =
+              l > 0.f ? m * 0.69314718055994531f + logf(l) : -INFINITY;
+      } else if (ntiles == 0 && in_window) {
 #pragma unroll
         for (int c = 0; c < D; c += 8)
           *reinterpret_cast<uint4*>(orow + c) = make_uint4(0, 0, 0, 0);
@@ -481,7 +489,7 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const int32_t* key_reach, const void* blockmap, int32_t T_pad,
                             int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o, float* lse,
-                            int32_t* status, cudaStream_t s) {
+                            int32_t* status, cudaStream_t s, int32_t row_lo, int32_t row_hi) {
   const int g = Hq / Hkv;
   FwdParams p;
   p.key_reach = key_reach;
@@ -496,7 +504,13 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.status = status;
-  const int grid = p.nb * p.n_hgroups;
+  p.row_lo = row_lo;
+  p.row_hi = row_hi;
+  p.windowed = (row_lo > 0 || row_hi < T_pad) ? 1 : 0;
+  p.qa_lo = row_lo / kBlock;
+  p.n_qa = row_hi > row_lo ? (row_hi - 1) / kBlock - p.qa_lo + 1 : 0;
+  if (p.n_qa == 0) return cudaSuccess;
+  const int grid = p.n_qa * p.n_hgroups;
   return d == 64 ? launch_fwd_d<64>(tq, tk, tv, p, grid, s)
                  : launch_fwd_d<128>(tq, tk, tv, p, grid, s);
 }

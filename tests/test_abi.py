@@ -98,6 +98,33 @@ def test_host_side_errors_return_before_launch():
 
 
 
+def test_dta_attn_checks_arguments_before_launch():
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    f = lib.tree_dta_attn
+    f.restype = ctypes.c_int
+    f.argtypes = [P] * 6 + [SZ, I32, I32, I32, I32, ctypes.c_float, P, I64] + [P] * 6 + \
+        [SZ, P, P]
+    T, Hq, Hkv, d = 256, 4, 2, 64
+    ws = ptg.dta_attn_workspace_bytes(T, Hq, Hkv, d)
+    assert ws == ptg.attn_bwd_workspace_bytes(T, Hq, d) + 2 * T * Hkv * d * 4
+
+    def call(ops, n=None, T=T, ws_bytes=ws, bm_bytes=1 << 20, d=d):
+        arr = np.ascontiguousarray(np.asarray(ops, np.int32).reshape(-1, 3))
+        return f(*([FAKE] * 6), bm_bytes, T, Hq, Hkv, d, 0.125,
+                 arr.ctypes.data if arr.size else None, arr.shape[0] if n is None else n,
+                 *([FAKE] * 6), ws_bytes, FAKE, None)
+    assert call([[3, 0, 8]]) == 1                # unknown op kind
+    assert call([[0, 8, 8]]) == 1                # empty row range
+    assert call([[1, 0, T + 1]]) == 1            # past T_pad
+    assert call([[2, -1, 4]]) == 1               # negative start
+    assert call([[0, 0, 8]], n=-1) == 1          # negative count
+    assert call([[0, 0, 8]], ws_bytes=ws - 16) == 8
+    assert call([[0, 0, 8]], bm_bytes=16) == 8
+    assert call([[0, 0, 8]], T=200) == 2
+    assert call([[0, 0, 8]], d=96) == 5
+    assert call([], T=0) == 0                    # empty input is a no-op
+
+
 def test_logprob_entry_points_check_arguments_before_launch():
     P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     f = lib.tree_logprobs_entropy

@@ -15,9 +15,11 @@ visible pairs count only unmasked (i, j) over real tokens (4 d Hq per pair
 for the forward, 10 d Hq for the backward).  Packed tokens/s is reported too.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--split replicas|balanced] [--path attention|logprob]
+                       [--split replicas|balanced] [--path attention|logprob|dta]
 --path logprob times the tree-aware log-probability / entropy gather over the
-same batch instead (bf16 logits over the Qwen3 vocabulary; its own JSON line).
+same batch instead (bf16 logits over the Qwen3 vocabulary; its own JSON line);
+--path dta runs the attention through the depth-first traversal schedule of
+dynamic tree attention (--chunk tokens per op) beside the packed step.
 Under torchrun each rank runs its own batch (seed = rank, --split replicas,
 the default): weak scaling, no collective on the data path.  With --split
 balanced every rank takes the same global batch and keeps one group of the
@@ -601,6 +603,99 @@ def run_ours(args, rank, ws):
         print(json.dumps(line), flush=True)
 
 
+def run_dta(args, rank, ws):
+    """``--path dta``: attention forward + backward executed through the
+    depth-first traversal of dynamic tree attention (AREAL-DTA 3.1-3.2), one
+    ``tree_dta_attn`` call per trie with its schedule at ``--chunk`` tokens,
+    against the packed step on the same batch in the same run.  One step =
+    for every trie: positions, blockmap, then the schedule's ops.  Same
+    metric as the packed path (effective TFLOP/s over visible pairs)."""
+    import torch
+    import prefix_tree_attention_gb300 as ptg
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    wl, seqs, cases = build_cases(ptg, args.workload, args.seed, rank, ws, args.split,
+                                  args.tries, device)
+    stats = workload_stats(wl, seqs, cases)
+    t_sched = time.perf_counter()
+    scheds = [ptg.dta_schedule(c.tr.token_node, c.tr.node_entry, c.tr.node_exit, args.chunk)
+              for c in cases]
+    sched_s = time.perf_counter() - t_sched
+    n_ops = sum(len(o) for o, _ in scheds)
+    peak = max(pk for _, pk in scheds)
+    ws_bytes = max(ptg.dta_attn_workspace_bytes(c.T, wl.Hq, wl.Hkv, wl.d) for c in cases)
+    wsp = torch.empty((ws_bytes + 3) // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for c, (ops, _pk) in zip(cases, scheds):
+            b = c.bufs
+            ptg.tree_pack_positions(c.token_node, c.entry, c.exit, b.position_ids, b.key_reach,
+                                    b.pos_ws, b.status)
+            ptg.tree_blockmap_build(b.key_reach, b.blockmap, b.status)
+            ptg.tree_dta_attn(c.q, c.k, c.v, c.do, b.key_reach, b.blockmap, ops, c.o, c.lse,
+                              c.dq, c.dk, c.dv, wsp, b.status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bad = [int(c.bufs.status.item()) for c in cases]
+    if any(bad):
+        raise RuntimeError("device status " + ptg.status_string(max(bad)))
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    launches0 = ptg.launch_count()
+    barrier(ws)
+    torch.cuda.synchronize()
+    per_step = []
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            s0, s1 = mk(), mk()
+            s0.record(stream)
+            step()
+            s1.record(stream)
+            per_step.append((s0, s1))
+        torch.cuda.synchronize()
+    barrier(ws)
+    launches = ptg.launch_count() - launches0
+    ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in per_step])), ws)
+    # the packed step on the same tries, same run (one stream, as the DTA step)
+    st = Stepper(ptg, cases, wl, 1, device)
+    for _ in range(3):
+        st.step()
+    packed_ms = max_over_ranks(float(np.mean(st.timed(args.steps))), ws)
+    st.check_status("in the packed comparison")
+    flops_all = sum_over_ranks(stats["flops"], ws)
+    peaks = measured_peaks()
+    value = flops_all / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "strong" if (args.split == "balanced" and ws > 1) else "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": args.workload + (f" (first {args.tries} tries)" if args.tries else ""),
+            "path": "dta", "chunk": args.chunk, "tries": len(cases),
+            "visible_pairs": stats["pairs"], "packed_tokens": stats["tokens"],
+            "ops_per_step": n_ops, "peak_stack_tokens": peak,
+            "largest_trie_tokens": max(c.T for c in cases),
+            "schedule_host_ms": round(sched_s * 1e3, 2),
+            "packed_ms_per_step_same_run": round(packed_ms, 3),
+            "packed_tflops_same_run": round(flops_all / (packed_ms * 1e-3) / 1e12, 2),
+            "dta_over_packed_time": round(ms / packed_ms, 4),
+            "frac_of_bf16_peak": round(value / peaks["bf16"], 4),
+            "l2": "inputs larger than L2 (no flush needed)",
+        },
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 LOGPROB_METRIC = "tree log-prob/entropy gather of packed logits, packed tokens/s"
 QWEN3_VOCAB = 151936
 
@@ -897,9 +992,12 @@ def main(argv=None):
                          "load-balanced partitioner")
     ap.add_argument("--streams", type=int, default=2,
                     help="CUDA streams the independent tries of a batch alternate over")
-    ap.add_argument("--path", choices=["attention", "logprob"], default="attention",
+    ap.add_argument("--path", choices=["attention", "logprob", "dta"], default="attention",
                     help="attention: the fwd+bwd step (default); logprob: the tree-aware "
-                         "log-prob / entropy gather over packed logits")
+                         "log-prob / entropy gather over packed logits; dta: the same "
+                         "attention executed through the depth-first traversal schedule")
+    ap.add_argument("--chunk", type=int, default=2048,
+                    help="--path dta: chunk length of the traversal schedule")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the timed agent / long / fanout entries of config.per_workload")
@@ -914,6 +1012,8 @@ def main(argv=None):
         run_reference(args, rank, ws)
     elif args.path == "logprob":
         run_logprob(args, rank, ws)
+    elif args.path == "dta":
+        run_dta(args, rank, ws)
     else:
         run_ours(args, rank, ws)
     if ws > 1:

@@ -51,6 +51,8 @@ FWD_FLOPS_PER_PAIR = 4      # times d * Hq
 BWD_FLOPS_PER_PAIR = 10
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "bwd_main_traffic.json")
 KERNEL_SOURCE = os.path.join(ROOT, "prefix_tree_attention_gb300", "csrc", "attn_bwd.cu")
+LOGPROB_TRAFFIC = os.path.join(ROOT, "profiles", "logprob_row_stats_traffic.json")
+LOGPROB_SOURCE = os.path.join(ROOT, "prefix_tree_attention_gb300", "csrc", "logprob.cu")
 
 
 # ------------------------------------------------------------------ helpers
@@ -80,6 +82,19 @@ def measured_peaks():
 def source_hash(path: str) -> str:
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_logprob_traffic_per_row():
+    """DRAM bytes per real packed row of the log-prob row kernel, from a
+    committed ncu summary of a smaller case; None when absent or taken on a
+    different kernel source."""
+    if not os.path.exists(LOGPROB_TRAFFIC):
+        return None
+    with open(LOGPROB_TRAFFIC) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_sha256_16") != source_hash(LOGPROB_SOURCE):
+        return None
+    return rec["dram_bytes_captured_launch"] / rec["real_rows_captured_launch"]
 
 
 def recorded_traffic():
@@ -800,6 +815,7 @@ def run_logprob(args, rank, ws):
         row_ms += e0.elapsed_time(e1)
     row_bytes = sum(tr.n_tokens * (V * 2 + 8) + tr.T_pad * 4 for tr in tries)
     peaks = measured_peaks()
+    per_row = recorded_logprob_traffic_per_row()
     achieved = row_bytes / (row_ms * 1e-3) / 1e9
     line = {
         "metric": LOGPROB_METRIC, "value": round(tokens_all / (ms_max * 1e-3), 1),
@@ -820,7 +836,10 @@ def run_logprob(args, rank, ws):
             "kernel": "k_row_stats (row log-sum-exp / entropy)", "bound": "hbm",
             "achieved": round(achieved, 1), "peak": peaks["hbm"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm"], 4),
-            "peak_kind": f"HBM copy ({peaks['source']})", "traffic": None,
+            "peak_kind": f"HBM copy ({peaks['source']})",
+            "traffic": (None if per_row is None
+                        else round(per_row * tokens / len(cases), 1)),
+            "traffic_note": "ncu DRAM bytes of a tiny-workload launch scaled by real rows",
             "avg_launch_ms": round(row_ms / len(cases), 4),
             "bytes_per_launch": row_bytes / len(cases),
         },

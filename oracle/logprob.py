@@ -43,8 +43,12 @@ log_softmax), by closed forms (uniform logits; one dominant logit), by brute
 force over small tries (the predecessor from parent pointers is the last
 visible key before the token in the dense ancestor mask), and by the cache
 count (every non-root-start token is a label exactly once); the slice
-combination against scipy's logsumexp and entropy of the whole row.  See
-tests/test_oracle_logprob.py.
+combination against scipy's logsumexp and entropy of the whole row.  The
+backward (``gather_packed_tree_backward``, the gradient a training step takes
+through the gather) is pinned by float64 torch autograd through the
+per-sequence computation on the unpacked rows, by central differences of the
+forward on tiny tries, and by closed forms (uniform rows; rows of the
+gradient sum to zero).  See tests/test_oracle_logprob.py.
 """
 from __future__ import annotations
 
@@ -219,3 +223,66 @@ def combine_vocab_slices(stats) -> tuple[float, float, float, float]:
     w = np.exp(lses - lse)
     ent = float((w * (np.array([s[1] for s in stats]) + lse - lses)).sum())
     return float(lse), ent, float(min(s[2] for s in stats)), float(max(s[3] for s in stats))
+
+
+def sequence_pairs(packed, sid: int) -> list[tuple[int, int]]:
+    """(predicting row, label row) of every entry of sequence ``sid``, in the
+    order of steps 2 and 4: a node's internal pairs (r, r + 1) for r in
+    start .. end-1, then the transition (end, next node's start)."""
+    pairs: list[tuple[int, int]] = []
+    nodes = path_nodes(packed, sid)
+    for a, n in enumerate(nodes):
+        start, end = int(packed.node_start[n]), int(packed.node_end[n])
+        pairs.extend((r, r + 1) for r in range(start, end))
+        if a + 1 < len(nodes):
+            pairs.append((end, int(packed.node_start[nodes[a + 1]])))
+    return pairs
+
+
+def gather_packed_tree_backward(logits, packed, grads) -> np.ndarray:
+    """Gradient of the gather with respect to the packed logits, float64.
+
+    ``grads`` maps a sequence id to ``(g_lp, g_ent)``, the gradients of a
+    loss with respect to that sequence's log-probability and entropy vectors
+    (each of length L-1, or None for zero).  The page's gather is
+    differentiable end to end: a piece served from a cache passes back the
+    sum over every sequence that used it, so the walk below adds each
+    sequence's entries to its predicting rows one by one.  Entry t, taken at
+    row p with label y, adds
+        g_lp[t]  * (onehot(y) - q)                   d logprob / d x_p
+        g_ent[t] * (-q * (log q + H_p))              d entropy / d x_p
+    with q = softmax(x_p) and H_p its entropy (the derivative of
+    -sum q log q, using sum q = 1).  Rows that predict nothing stay 0.
+    """
+    x = np.asarray(logits, dtype=np.float64)
+    out = np.zeros_like(x)
+    tok = packed.token_ids
+    for sid, (g_lp, g_ent) in grads.items():
+        for t, (p, lab) in enumerate(sequence_pairs(packed, sid)):
+            lq = log_softmax(x[p])
+            q = np.exp(lq)
+            if g_lp is not None:
+                out[p] -= g_lp[t] * q
+                out[p, tok[lab]] += g_lp[t]
+            if g_ent is not None:
+                h = -(q * lq).sum()
+                out[p] -= g_ent[t] * q * (lq + h)
+    return out
+
+
+def merge_packed_tree_results_backward(grad_out, results) -> list[dict]:
+    """Adjoint of ``merge_packed_tree_results``: the merged gradient
+    ``[n_seqs, max_len]`` back into each micro-batch's ``{sid: vector}``
+    (entries past a sequence's length, or past max_len, receive nothing)."""
+    g = np.asarray(grad_out, dtype=np.float64)
+    out = []
+    for res in results:
+        part = {}
+        for sid, vec in res.items():
+            n = np.asarray(vec).size
+            v = np.zeros(n, np.float64)
+            k = min(n, g.shape[1])
+            v[:k] = g[sid, :k]
+            part[sid] = v
+        out.append(part)
+    return out

@@ -213,3 +213,128 @@ def test_vocab_parallel_combine_equals_whole_row(V, n):
     got = OL.combine_vocab_slices(parts)
     want = (logsumexp(x), sp_entropy(softmax(x)), x.min(), x.max())
     np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------------ backward
+def _seq_grads(packed, seed, lp=True, ent=True):
+    """Random gradients of a loss with respect to every sequence's
+    log-probability and entropy vectors."""
+    rng = np.random.default_rng(seed)
+    out = {}
+    for sid in packed.seq_ids:
+        n = len(packed.seq_index[sid]) - 1
+        out[sid] = (rng.standard_normal(n) if lp else None,
+                    rng.standard_normal(n) if ent else None)
+    return out
+
+
+def _autograd_unpacked(logits, packed, grads):
+    """d loss / d logits by float64 torch autograd through the per-sequence
+    computation on the sequence's own rows (torch's log_softmax and the
+    Categorical entropy), with loss = sum over sequences of
+    g_lp . logprob + g_ent . entropy."""
+    import torch
+    X = torch.tensor(logits, dtype=torch.float64, requires_grad=True)
+    loss = X.new_zeros(())
+    for sid, (g_lp, g_ent) in grads.items():
+        idx = np.asarray(packed.seq_index[sid])
+        rows = X[torch.as_tensor(idx[:-1])]
+        labels = torch.as_tensor(packed.token_ids[idx[1:]].astype(np.int64))
+        if g_lp is not None:
+            lp = torch.log_softmax(rows, dim=1).gather(1, labels[:, None])[:, 0]
+            loss = loss + (torch.as_tensor(g_lp) * lp).sum()
+        if g_ent is not None:
+            ent = torch.distributions.Categorical(logits=rows).entropy()
+            loss = loss + (torch.as_tensor(g_ent) * ent).sum()
+    loss.backward()
+    return X.grad.numpy()
+
+
+def test_backward_equals_autograd_of_unpacked_sequences():
+    rng = W.SplitMix64(99)
+    for trial in range(6):
+        seqs = W.random_sequences(rng, rng.randint(2, 9), 40, 3)
+        V = 23 + 7 * trial
+        for t in OT.pack_sequences(seqs, 1024):
+            logits = _logits(t.T_pad, V, trial + 40)
+            for lp, ent in ((True, True), (True, False), (False, True)):
+                grads = _seq_grads(t, trial, lp, ent)
+                got = OL.gather_packed_tree_backward(logits, t, grads)
+                want = _autograd_unpacked(logits, t, grads)
+                np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def _loss(logits, packed, grads):
+    res, _ = OL.gather_packed_tree_logprobs_entropy(logits, packed)
+    tot = 0.0
+    for sid, (g_lp, g_ent) in grads.items():
+        lp, ent = res[sid]
+        tot += float(np.dot(g_lp, lp)) + float(np.dot(g_ent, ent))
+    return tot
+
+
+def test_backward_central_differences():
+    seqs = [[1, 2, 3, 4], [1, 2, 5], [1, 6], [7, 3]]
+    (t,) = OT.pack_sequences(seqs, 128)
+    V = 7
+    logits = _logits(t.T_pad, V, 11)
+    grads = _seq_grads(t, 5)
+    got = OL.gather_packed_tree_backward(logits, t, grads)
+    h = 1e-5
+    for r in range(t.n_tokens):
+        for v in range(V):
+            a, b = logits.copy(), logits.copy()
+            a[r, v] += h
+            b[r, v] -= h
+            fd = (_loss(a, t, grads) - _loss(b, t, grads)) / (2 * h)
+            assert abs(fd - got[r, v]) < 1e-8, (r, v, fd, got[r, v])
+
+
+def test_backward_closed_forms():
+    # one sequence [1, 2, 3] over uniform rows: softmax is 1/V and the
+    # entropy is at its maximum, so its gradient vanishes
+    V = 9
+    (t,) = OT.pack_sequences([[1, 2, 3]], 128)
+    logits = np.full((t.T_pad, V), 0.75)
+    g = {0: (np.array([2.0, -3.0]), np.array([5.0, 7.0]))}
+    got = OL.gather_packed_tree_backward(logits, t, g)
+    want = np.zeros_like(logits)
+    want[0] = -2.0 / V
+    want[0, 2] += 2.0
+    want[1] = 3.0 / V
+    want[1, 3] -= 3.0
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-14)
+    # rows of the gradient sum to zero (softmax sums to 1) and pads and
+    # rows that predict nothing get nothing
+    rng = W.SplitMix64(8)
+    seqs = W.random_sequences(rng, 6, 30, 2)
+    (t,) = OT.pack_sequences(seqs, 2048)
+    logits = _logits(t.T_pad, 31, 2)
+    got = OL.gather_packed_tree_backward(logits, t, _seq_grads(t, 3))
+    np.testing.assert_allclose(got.sum(axis=1), 0.0, atol=1e-12)
+    predicting = np.zeros(t.T_pad, bool)
+    predicting[OL.token_pred(t)[OL.token_pred(t) >= 0]] = True
+    assert (got[~predicting] == 0).all()
+    # the two-point row [0, ln 3] (p = 1/4, 3/4): d H / d x_0 = p0 p1 ln(p1/p0)
+    (t,) = OT.pack_sequences([[0, 1]], 128)
+    logits = np.zeros((t.T_pad, 2))
+    logits[0, 1] = np.log(3.0)
+    got = OL.gather_packed_tree_backward(logits, t, {0: (None, np.array([1.0]))})
+    assert abs(got[0, 0] - 0.1875 * np.log(3.0)) < 1e-15
+    assert abs(got[0, 1] + 0.1875 * np.log(3.0)) < 1e-15
+
+
+def test_merge_backward_is_the_adjoint():
+    rng = np.random.default_rng(4)
+    res = [{0: rng.standard_normal(3), 1: rng.standard_normal(2)},
+           {2: rng.standard_normal(1), 3: rng.standard_normal(5)}]
+    for max_len in (None, 3):
+        fwd = OL.merge_packed_tree_results(res, 4, padding_value=1.5, max_len=max_len)
+        g = rng.standard_normal(fwd.shape)
+        back = OL.merge_packed_tree_results_backward(g, res)
+        # <merge(x) - merge(0), g> = sum over parts <x, merge^T g>
+        zero = [{s: np.zeros_like(v) for s, v in part.items()} for part in res]
+        lin = fwd - OL.merge_packed_tree_results(zero, 4, padding_value=1.5, max_len=max_len)
+        lhs = float((lin * g).sum())
+        rhs = sum(float(np.dot(part[s], bp[s])) for part, bp in zip(res, back) for s in part)
+        assert abs(lhs - rhs) < 1e-12

@@ -169,6 +169,52 @@ def test_predecessor_at_the_parent_start_is_caught(monkeypatch):
         TL.test_brute_force_predecessors_exhaustive_pairs()
 
 
+def _gather_backward_variant(mistake):
+    """The gather backward with one mistake."""
+    def bwd(logits, packed, grads):
+        x = np.asarray(logits, dtype=np.float64)
+        out = np.zeros_like(x)
+        tok = packed.token_ids
+        for sid, (g_lp, g_ent) in grads.items():
+            for t, (p, lab) in enumerate(OL.sequence_pairs(packed, sid)):
+                lq = OL.log_softmax(x[p])
+                q = np.exp(lq)
+                row = lab if mistake == "label_row" else p
+                if g_lp is not None:
+                    if mistake != "no_softmax_term":
+                        out[row] -= g_lp[t] * q
+                    out[row, tok[lab]] += g_lp[t]
+                if g_ent is not None:
+                    h = -(q * lq).sum()
+                    sign = -1.0 if mistake == "entropy_sign" else 1.0
+                    out[row] -= g_ent[t] * q * (lq + sign * h)
+        return out
+    return bwd
+
+
+@pytest.mark.parametrize("mistake", ["label_row", "no_softmax_term", "entropy_sign"])
+def test_gather_backward_mistakes_are_caught(monkeypatch, mistake):
+    monkeypatch.setattr(OL, "gather_packed_tree_backward", _gather_backward_variant(mistake))
+    with pytest.raises(AssertionError):
+        TL.test_backward_equals_autograd_of_unpacked_sequences()
+    with pytest.raises(AssertionError):
+        TL.test_backward_closed_forms()
+
+
+def test_unmodified_gather_backward_variant_passes(monkeypatch):
+    monkeypatch.setattr(OL, "gather_packed_tree_backward", _gather_backward_variant(None))
+    TL.test_backward_equals_autograd_of_unpacked_sequences()
+    TL.test_backward_closed_forms()
+
+
+def test_backward_without_transitions_is_caught(monkeypatch):
+    orig = OL.sequence_pairs
+    monkeypatch.setattr(OL, "sequence_pairs", lambda packed, sid: [
+        (p, l) for p, l in orig(packed, sid) if l == p + 1])
+    with pytest.raises(AssertionError):
+        TL.test_backward_equals_autograd_of_unpacked_sequences()
+
+
 # ------------------------------------------------------------ DTA schedule
 def test_shallowest_first_order_is_caught(monkeypatch):
     monkeypatch.setattr(OD, "greedy_order", lambda nodes, depth, packed: sorted(

@@ -815,6 +815,9 @@ def run_logprob(args, rank, ws):
         row_ms += e0.elapsed_time(e1)
     row_bytes = sum(tr.n_tokens * (V * 2 + 8) + tr.T_pad * 4 for tr in tries)
     peaks = measured_peaks()
+    backward = None if args.no_extra else logprob_backward(
+        ptg, cases, offs, logits, lse_all, ent_all, pos_d, soffs_d, (len(used), max_len), V,
+        tokens, seed, args, ws, peaks)
     per_row = recorded_logprob_traffic_per_row()
     achieved = row_bytes / (row_ms * 1e-3) / 1e9
     line = {
@@ -846,6 +849,7 @@ def run_logprob(args, rank, ws):
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "e2e": None,
+        "backward": backward,
     }
     if rank == 0 and not args.no_cpu_baseline:
         rate, desc = logprob_oracle_rate(min(args.cpu_budget, 10.0), seed)
@@ -853,6 +857,96 @@ def run_logprob(args, rank, ws):
                                 "kind": "oracle", "sample": desc}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def logprob_backward(ptg, cases, offs, logits, lse_all, ent_all, pos_d, soffs_d, merged_shape,
+                     V, tokens, seed, args, ws, peaks):
+    """The gather's gradient over the same batch, timed apart from the
+    forward: per-sequence gradients of log-probabilities and entropies
+    ([n_seqs, max_len], fp32 N(0, 1)) go back through the two merge adjoints
+    (tree_merge_per_sequence_bwd) to packed per-token / per-row gradients,
+    then tree_logprobs_entropy_bwd writes the bf16 logits gradient of every
+    trie, reading its logits once more.  Returns the ``backward`` object of
+    the log-prob line: its own rate and the row kernel's HBM roofline."""
+    import torch
+    device = logits.device
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 + seed)
+    g_lp = torch.randn(merged_shape, generator=g, device=device, dtype=torch.float32)
+    g_ent = torch.randn(merged_shape, generator=g, device=device, dtype=torch.float32)
+    total = offs[-1]
+    tok_g = torch.empty(total, dtype=torch.float32, device=device)
+    row_g = torch.empty_like(tok_g)
+    grad = torch.empty_like(logits)            # one gradient buffer, like the logits
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def rows(i, tr, bufs, tok):
+        sl = slice(offs[i], offs[i + 1])
+        ptg.tree_logprobs_entropy_bwd(logits[:tr.T_pad], bufs.key_reach, lse_all[sl],
+                                      grad[:tr.T_pad], bufs.status, token_ids=tok,
+                                      entropy=ent_all[sl], grad_logprob=tok_g[sl],
+                                      grad_entropy=row_g[sl])
+
+    def step():
+        tok_g.zero_()
+        row_g.zero_()
+        ptg.tree_merge_per_sequence_bwd(g_lp, pos_d, soffs_d, tok_g, status, 1, 1)
+        ptg.tree_merge_per_sequence_bwd(g_ent, pos_d, soffs_d, row_g, status, 0, 1)
+        for i, (tr, bufs, tok) in enumerate(cases):
+            rows(i, tr, bufs, tok)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bad = [int(b.status.item()) for _, b, _ in cases] + [int(status.item())]
+    if any(bad):
+        raise RuntimeError("device status " + ptg.status_string(max(bad)))
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    launches0 = ptg.launch_count()
+    barrier(ws)
+    torch.cuda.synchronize()
+    per_step = []
+    for _ in range(args.steps):
+        s0, s1 = mk(), mk()
+        s0.record(stream)
+        step()
+        s1.record(stream)
+        per_step.append((s0, s1))
+    torch.cuda.synchronize()
+    barrier(ws)
+    launches = ptg.launch_count() - launches0
+    ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in per_step])), ws)
+    # the row kernel alone, each launch bracketed by events
+    row_ms = 0.0
+    for i, (tr, bufs, tok) in enumerate(cases):
+        e0, e1 = mk(), mk()
+        e0.record(stream)
+        rows(i, tr, bufs, tok)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        row_ms += e0.elapsed_time(e1)
+    # per real row: V logits read, V gradients written (bf16), lse, entropy,
+    # reach, the row's entropy gradient, its children's gradients; a pad row
+    # writes its V zeros
+    bwd_bytes = sum(tr.n_tokens * (V * 4 + 24) + (tr.T_pad - tr.n_tokens) * (V * 2 + 4)
+                    for tr, _, _ in cases)
+    achieved = bwd_bytes / (row_ms * 1e-3) / 1e9
+    return {
+        "what": "merge adjoints (log-prob, entropy) + logits gradient of every trie",
+        "ms_per_step": round(ms, 3),
+        "tokens_per_s": round(sum_over_ranks(tokens, ws) / (ms * 1e-3), 1),
+        "gpu_launches": launches,
+        "roofline": {
+            "kernel": "k_row_bwd (logits gradient)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": peaks["hbm"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm"], 4),
+            "peak_kind": f"HBM copy ({peaks['source']})",
+            "traffic": None,
+            "avg_launch_ms": round(row_ms / len(cases), 4),
+            "bytes_per_launch": bwd_bytes / len(cases),
+        },
+    }
 
 
 def run_e2e(ptg, cases, ws_bwds, streams, args, ws, flops_all):
@@ -1019,7 +1113,8 @@ def main(argv=None):
                     help="--path dta: chunk length of the traversal schedule")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the timed agent / long / fanout entries of config.per_workload")
+                    help="skip the timed agent / long / fanout entries of config.per_workload "
+                         "and the backward object of the log-prob line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")

@@ -441,6 +441,89 @@ TREE_API tree_status_t tree_merge_per_sequence(const float* src, int64_t n_src,
                                                int32_t* dev_status, tree_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * tree_merge_per_sequence_bwd — the merge's adjoint (its gradient).
+ *
+ * Source: the same section; the page's merge is part of a differentiable
+ * computation, so a training step passes the gradient of its loss with
+ * respect to the merged [n_seqs, max_len] batch back to the packed values.
+ * With the arguments of the forward call (same seq_pos, seq_offsets, shift,
+ * trim, max_len):
+ *     src_grad[seq_pos[seq_offsets[s] + t + shift]] += out_grad[s, t]
+ *                                                   for t < min(L - trim, max_len).
+ * A packed token shared by several sequences (a common prefix) receives the
+ * sum over those sequences.  ACCUMULATES into src_grad: zero it first for a
+ * plain gradient.  The sums use fp32 atomic adds, so their rounding order,
+ * and the last bits of a shared token's sum, may differ run to run.
+ *
+ *   out_grad     [in]  device float[n_seqs * max_len]
+ *   seq_pos, n_pos, seq_offsets, n_seqs, max_len, shift, trim
+ *                [in]  as in tree_merge_per_sequence
+ *   src_grad     [in,out] device float[n_src]
+ *   dev_status   [out] TREE_ERR_MALFORMED_TREE for an index outside
+ *                      [0, n_src), TREE_ERR_INVALID_ARG for bad offsets,
+ *                      TREE_ERR_CAPACITY if L - trim > max_len (the entries
+ *                      that fit are still added); offending entries add nothing
+ * Returns TREE_ERR_INVALID_ARG for negative sizes, shift < 0 or
+ * trim < shift, or a missing pointer.  n_seqs == 0 or max_len == 0 is a
+ * no-op.  One launch.
+ * ---------------------------------------------------------------------- */
+TREE_API tree_status_t tree_merge_per_sequence_bwd(const float* out_grad, const int32_t* seq_pos,
+                                                   int64_t n_pos, const int64_t* seq_offsets,
+                                                   int32_t n_seqs, int32_t max_len,
+                                                   int32_t shift, int32_t trim, float* src_grad,
+                                                   int64_t n_src, int32_t* dev_status,
+                                                   tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * tree_logprobs_entropy_bwd — gradient of the gather with respect to the logits.
+ *
+ * Source: the section "Log Probability 计算：树结构的特殊处理" of the guide;
+ * its gather is differentiated by a training step's backward pass.  Inputs
+ * are the per-token gradients in the packed layout (as
+ * tree_merge_per_sequence_bwd leaves them): grad_logprob[j], the gradient
+ * with respect to logprob[j] of tree_logprobs_entropy (label token j), and
+ * grad_entropy[r], with respect to entropy[r] (row r).  With p = softmax
+ * of row r, H = entropy[r], and the children of r (the tokens j with
+ * pred(j) = r, each with its label y_j = token_ids[j]):
+ *     grad_logits[r, v] = sum_{pred(j) = r} grad_logprob[j] * ([v == y_j] - p_v)
+ *                       - grad_entropy[r] * p_v * (logits[r, v] - lse[r] + H)
+ * (d log p_y / d x_v = [v == y] - p_v;  d H / d x_v = -p_v (log p_v + H)).
+ * Pad rows get 0.  Overwrites grad_logits (rows [0, T_pad), first V
+ * entries each).  fp32 arithmetic with the hardware 2^x approximation,
+ * one rounding to the output type per entry; deterministic.  Uses the lse
+ * and entropy saved by tree_logprobs_entropy on the same logits; the
+ * children of r are found from key_reach (r + 1, then each next sibling
+ * at key_reach[j] + 1, while j <= key_reach[r]), so no pred array is needed.
+ *
+ *   logits        [in]  device, as in tree_logprobs_entropy (same dtype and layout)
+ *   token_ids     [in]  device int32[T_pad] (needed when grad_logprob != NULL)
+ *   key_reach     [in]  device int32[T_pad] from tree_pack_positions
+ *   lse           [in]  device float[T_pad] from tree_logprobs_entropy
+ *   entropy       [in]  device float[T_pad] from tree_logprobs_entropy
+ *                       (needed when grad_entropy != NULL)
+ *   grad_logprob  [in]  device float[T_pad] per label token, or NULL (zero)
+ *   grad_entropy  [in]  device float[T_pad] per row, or NULL (zero)
+ *   grad_logits   [out] device [T_pad rows, grad_row_stride elements] of
+ *                       the logits' dtype; rows 16-byte aligned with the
+ *                       logits' rows are written in 16-byte groups
+ *   dev_status    [out] TREE_ERR_MALFORMED_TREE if a child's id is outside
+ *                       [0, V) (its one-hot term is dropped)
+ * Returns TREE_ERR_UNSUPPORTED for another dtype, TREE_ERR_INVALID_ARG for a
+ * missing required pointer, V < 1 or a row stride < V, TREE_ERR_ALIGNMENT if
+ * T_pad % 128 != 0.  T_pad == 0 is a no-op.  One launch, one CTA per row:
+ * reads and writes each row's V values once.
+ * ---------------------------------------------------------------------- */
+TREE_API tree_status_t tree_logprobs_entropy_bwd(const void* logits, int32_t dtype,
+                                                 int64_t row_stride, int32_t T_pad, int32_t V,
+                                                 const int32_t* token_ids,
+                                                 const int32_t* key_reach, const float* lse,
+                                                 const float* entropy,
+                                                 const float* grad_logprob,
+                                                 const float* grad_entropy, void* grad_logits,
+                                                 int64_t grad_row_stride, int32_t* dev_status,
+                                                 tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * tree_dta_schedule — the depth-first traversal of dynamic tree attention.
  *
  * Source: AREAL-DTA, sections 3.1 (DFS over the prefix tree with a stack of

@@ -239,7 +239,7 @@ def sequence_pairs(packed, sid: int) -> list[tuple[int, int]]:
     return pairs
 
 
-def gather_packed_tree_backward(logits, packed, grads) -> np.ndarray:
+def gather_packed_tree_backward(logits, packed, grads, rows=None):
     """Gradient of the gather with respect to the packed logits, float64.
 
     ``grads`` maps a sequence id to ``(g_lp, g_ent)``, the gradients of a
@@ -253,21 +253,37 @@ def gather_packed_tree_backward(logits, packed, grads) -> np.ndarray:
         g_ent[t] * (-q * (log q + H_p))              d entropy / d x_p
     with q = softmax(x_p) and H_p its entropy (the derivative of
     -sum q log q, using sum q = 1).  Rows that predict nothing stay 0.
+
+    Returns the dense ``[T_pad, V]`` gradient; with ``rows`` (row indices)
+    only the entries at those predicting rows are taken and a dict
+    ``{row: gradient row}`` is returned, and ``logits`` need only support
+    ``logits[row]`` for them (so large logits can stay where they are).
     """
-    x = np.asarray(logits, dtype=np.float64)
-    out = np.zeros_like(x)
+    want = None if rows is None else {int(r) for r in rows}
     tok = packed.token_ids
+    acc: dict[int, np.ndarray] = {}
+    lsm: dict[int, np.ndarray] = {}
     for sid, (g_lp, g_ent) in grads.items():
         for t, (p, lab) in enumerate(sequence_pairs(packed, sid)):
-            lq = log_softmax(x[p])
+            if want is not None and p not in want:
+                continue
+            if p not in lsm:
+                lsm[p] = log_softmax(np.asarray(logits[p], dtype=np.float64))
+            lq = lsm[p]
             q = np.exp(lq)
+            out = acc.setdefault(p, np.zeros_like(lq))
             if g_lp is not None:
-                out[p] -= g_lp[t] * q
-                out[p, tok[lab]] += g_lp[t]
+                out -= g_lp[t] * q
+                out[tok[lab]] += g_lp[t]
             if g_ent is not None:
                 h = -(q * lq).sum()
-                out[p] -= g_ent[t] * q * (lq + h)
-    return out
+                out -= g_ent[t] * q * (lq + h)
+    if want is not None:
+        return {r: acc.get(r, np.zeros(np.asarray(logits[r]).shape[-1])) for r in sorted(want)}
+    dense = np.zeros(np.shape(logits), dtype=np.float64)
+    for p, v in acc.items():
+        dense[p] = v
+    return dense
 
 
 def merge_packed_tree_results_backward(grad_out, results) -> list[dict]:

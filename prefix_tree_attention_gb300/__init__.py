@@ -9,7 +9,8 @@ Entry points mirror the C ABI names: ``tree_pack_positions``,
 ``tree_blockmap_build``, ``tree_attn_fwd``, ``tree_attn_bwd`` (each takes
 tensors, checks their dtype/shape/device, passes raw pointers and the current
 CUDA stream, and raises ``TreeError`` on a non-OK status), the log-probability
-gather ``tree_logprobs_entropy`` with its merge ``tree_merge_per_sequence``,
+gather ``tree_logprobs_entropy`` with its merge ``tree_merge_per_sequence``
+and their gradients ``tree_logprobs_entropy_bwd`` / ``tree_merge_per_sequence_bwd``,
 plus the host packer ``pack_sequences``, partitioner ``partition_sequences``
 and the DFS traversal schedule ``dta_schedule``.
 """
@@ -62,6 +63,10 @@ _sig = {
                                              _P, _P, _P, _P, _P, _P, _P]),
     "tree_merge_per_sequence": (ctypes.c_int, [_P, _I64, _P, _I64, _P, _I32, _I32, _I32, _I32,
                                                _F32, _P, _P, _P]),
+    "tree_merge_per_sequence_bwd": (ctypes.c_int, [_P, _P, _I64, _P, _I32, _I32, _I32, _I32, _P,
+                                                   _I64, _P, _P]),
+    "tree_logprobs_entropy_bwd": (ctypes.c_int, [_P, _I32, _I64, _I32, _I32, _P, _P, _P, _P, _P,
+                                                 _P, _P, _I64, _P, _P]),
     "tree_dta_schedule": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _P]),
     "tree_dta_attn_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32]),
     "tree_dta_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _SZ, _I32, _I32, _I32, _I32, _F32,
@@ -300,6 +305,62 @@ def tree_merge_per_sequence(src, seq_pos, seq_offsets, out, dev_status, shift: i
         _ptr(src), src.numel(), _ptr(seq_pos), seq_pos.numel(), _ptr(seq_offsets), n_seqs,
         max_len, int(shift), int(trim), float(padding_value), _ptr(out), _ptr(dev_status),
         _stream_ptr(stream)))
+
+
+def tree_merge_per_sequence_bwd(out_grad, seq_pos, seq_offsets, src_grad, dev_status,
+                                shift: int, trim: int, stream=None):
+    """Adjoint of ``tree_merge_per_sequence`` with the same ``seq_pos``,
+    ``seq_offsets``, ``shift`` and ``trim``: ``src_grad[seq_pos[seq_offsets[s]
+    + t + shift]] += out_grad[s, t]``.  Accumulates: zero ``src_grad`` first."""
+    import torch
+    _on_device(out_grad=out_grad, seq_pos=seq_pos, seq_offsets=seq_offsets, src_grad=src_grad,
+               dev_status=dev_status)
+    _need(out_grad, torch.float32, "out_grad")
+    _need(seq_pos, torch.int32, "seq_pos")
+    _need(seq_offsets, torch.int64, "seq_offsets")
+    _need(src_grad, torch.float32, "src_grad")
+    if out_grad.dim() != 2:
+        raise ValueError("out_grad must be [n_seqs, max_len]")
+    n_seqs, max_len = out_grad.shape
+    if seq_offsets.numel() != n_seqs + 1:
+        raise ValueError("seq_offsets must hold n_seqs + 1 values")
+    _check("tree_merge_per_sequence_bwd", _lib.tree_merge_per_sequence_bwd(
+        _ptr(out_grad), _ptr(seq_pos), seq_pos.numel(), _ptr(seq_offsets), n_seqs, max_len,
+        int(shift), int(trim), _ptr(src_grad), src_grad.numel(), _ptr(dev_status),
+        _stream_ptr(stream)))
+
+
+def tree_logprobs_entropy_bwd(logits, key_reach, lse, grad_logits, dev_status, token_ids=None,
+                              entropy=None, grad_logprob=None, grad_entropy=None, stream=None):
+    """Gradient of the log-probability / entropy gather with respect to the
+    packed logits: ``grad_logits`` (same dtype and shape as ``logits``) from
+    the per-token ``grad_logprob`` and per-row ``grad_entropy`` (either may
+    be None), using the ``lse`` and ``entropy`` of the forward call."""
+    import torch
+    _on_device(logits=logits, key_reach=key_reach, lse=lse, grad_logits=grad_logits,
+               dev_status=dev_status, token_ids=token_ids, entropy=entropy,
+               grad_logprob=grad_logprob, grad_entropy=grad_entropy)
+    for t, n in ((logits, "logits"), (grad_logits, "grad_logits")):
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError(f"{n} must be 2-D with unit stride along the vocabulary")
+    code = {torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32}.get(logits.dtype)
+    if code is None:
+        raise TypeError(f"logits must be bf16 or float32, got {logits.dtype}")
+    if grad_logits.dtype != logits.dtype or grad_logits.shape != logits.shape:
+        raise ValueError("grad_logits must match the logits' dtype and shape")
+    T_pad, V = logits.shape
+    _need(key_reach, torch.int32, "key_reach")
+    for t, n in ((key_reach, "key_reach"), (lse, "lse"), (entropy, "entropy"),
+                 (grad_logprob, "grad_logprob"), (grad_entropy, "grad_entropy"),
+                 (token_ids, "token_ids")):
+        if t is not None:
+            _need(t, torch.int32 if n in ("key_reach", "token_ids") else torch.float32, n)
+            if t.numel() != T_pad:
+                raise ValueError(f"{n} must hold T_pad = {T_pad} values")
+    _check("tree_logprobs_entropy_bwd", _lib.tree_logprobs_entropy_bwd(
+        _ptr(logits), code, logits.stride(0), T_pad, V, _ptr(token_ids), _ptr(key_reach),
+        _ptr(lse), _ptr(entropy), _ptr(grad_logprob), _ptr(grad_entropy), _ptr(grad_logits),
+        grad_logits.stride(0), _ptr(dev_status), _stream_ptr(stream)))
 
 
 DTA_FWD_PUSH, DTA_FWD_BWD, DTA_BWD_POP = 0, 1, 2

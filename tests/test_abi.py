@@ -153,6 +153,34 @@ def test_logprob_entry_points_check_arguments_before_launch():
     assert m(FAKE, 10, FAKE, 10, FAKE, 0, 8, 1, 1, 0.0, FAKE, FAKE, None) == 0   # no-op
 
 
+
+def test_logprob_gradient_entry_points_check_arguments_before_launch():
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    f = lib.tree_logprobs_entropy_bwd
+    f.restype = ctypes.c_int
+    f.argtypes = [P, I32, I64, I32, I32, P, P, P, P, P, P, P, I64, P, P]
+
+    def call(dtype=0, stride=1000, T=256, V=1000, tok=FAKE, ent=FAKE, g_lp=FAKE, g_ent=FAKE,
+             out=FAKE, out_stride=1000, lse=FAKE, logits=FAKE):
+        return f(logits, dtype, stride, T, V, tok, FAKE, lse, ent, g_lp, g_ent, out, out_stride,
+                 FAKE, None)
+    assert call(dtype=2) == 5
+    assert call(V=0) == 1 and call(stride=999) == 1 and call(out_stride=999) == 1
+    assert call(T=200) == 2
+    assert call(logits=None) == 1 and call(lse=None) == 1 and call(out=None) == 1
+    assert call(tok=None) == 1                   # logprob gradient needs token ids
+    assert call(ent=None) == 1                   # entropy gradient needs the entropy
+    assert call(T=0) == 0 and call(T=0, logits=None) == 0   # empty input is a no-op
+    m = lib.tree_merge_per_sequence_bwd
+    m.restype = ctypes.c_int
+    m.argtypes = [P, P, I64, P, I32, I32, I32, I32, P, I64, P, P]
+    assert m(FAKE, FAKE, 10, FAKE, 2, 8, 1, 0, FAKE, 10, FAKE, None) == 1   # trim < shift
+    assert m(FAKE, FAKE, 10, FAKE, 2, 8, -1, 0, FAKE, 10, FAKE, None) == 1
+    assert m(FAKE, FAKE, 10, FAKE, 2, 8, 1, 1, FAKE, -1, FAKE, None) == 1
+    assert m(None, FAKE, 10, FAKE, 2, 8, 1, 1, FAKE, 10, FAKE, None) == 1
+    assert m(FAKE, FAKE, 10, FAKE, 2, 8, 1, 1, None, 10, FAKE, None) == 1
+    assert m(FAKE, FAKE, 10, FAKE, 0, 8, 1, 1, FAKE, 10, FAKE, None) == 0   # no-op
+
 def test_sequence_index_arrays_layout():
     tries = ptg.pack_sequences([[1, 2, 3], [1, 2, 4, 5], [7]], 128)
     pos, offs = ptg.sequence_index_arrays(tries, 3)

@@ -52,6 +52,7 @@ BWD_FLOPS_PER_PAIR = 10
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "bwd_main_traffic.json")
 KERNEL_SOURCE = os.path.join(ROOT, "prefix_tree_attention_gb300", "csrc", "attn_bwd.cu")
 LOGPROB_TRAFFIC = os.path.join(ROOT, "profiles", "logprob_row_stats_traffic.json")
+LOGPROB_BWD_TRAFFIC = os.path.join(ROOT, "profiles", "logprob_row_bwd_traffic.json")
 LOGPROB_SOURCE = os.path.join(ROOT, "prefix_tree_attention_gb300", "csrc", "logprob.cu")
 
 
@@ -84,13 +85,14 @@ def source_hash(path: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_logprob_traffic_per_row():
-    """DRAM bytes per real packed row of the log-prob row kernel, from a
+def recorded_logprob_traffic_per_row(path=LOGPROB_TRAFFIC):
+    """DRAM bytes per real packed row of a log-prob row kernel (the forward
+    row pass, or with ``LOGPROB_BWD_TRAFFIC`` the gradient's), from a
     committed ncu summary of a smaller case; None when absent or taken on a
     different kernel source."""
-    if not os.path.exists(LOGPROB_TRAFFIC):
+    if not os.path.exists(path):
         return None
-    with open(LOGPROB_TRAFFIC) as f:
+    with open(path) as f:
         rec = json.load(f)
     if rec.get("kernel_source_sha256_16") != source_hash(LOGPROB_SOURCE):
         return None
@@ -932,6 +934,8 @@ def logprob_backward(ptg, cases, offs, logits, lse_all, ent_all, pos_d, soffs_d,
     bwd_bytes = sum(tr.n_tokens * (V * 4 + 24) + (tr.T_pad - tr.n_tokens) * (V * 2 + 4)
                     for tr, _, _ in cases)
     achieved = bwd_bytes / (row_ms * 1e-3) / 1e9
+    per_row = recorded_logprob_traffic_per_row(LOGPROB_BWD_TRAFFIC)
+    real_rows = sum(tr.n_tokens for tr, _, _ in cases)
     return {
         "what": "merge adjoints (log-prob, entropy) + logits gradient of every trie",
         "ms_per_step": round(ms, 3),
@@ -942,7 +946,9 @@ def logprob_backward(ptg, cases, offs, logits, lse_all, ent_all, pos_d, soffs_d,
             "achieved": round(achieved, 1), "peak": peaks["hbm"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm"], 4),
             "peak_kind": f"HBM copy ({peaks['source']})",
-            "traffic": None,
+            "traffic": (None if per_row is None
+                        else round(per_row * real_rows / len(cases), 1)),
+            "traffic_note": "ncu DRAM bytes of a tiny-workload launch scaled by real rows",
             "avg_launch_ms": round(row_ms / len(cases), 4),
             "bytes_per_launch": bwd_bytes / len(cases),
         },

@@ -76,7 +76,9 @@ typedef enum {
   TREE_ERR_UNSUPPORTED = 5,    /* block != 128, head_dim not in {64,128} */
   TREE_ERR_CUDA = 6,           /* a CUDA call or launch failed */
   TREE_ERR_TIMEOUT = 7,        /* a device-side wait exceeded its limit (device-detected) */
-  TREE_ERR_WORKSPACE = 8       /* workspace or blockmap buffer too small */
+  TREE_ERR_WORKSPACE = 8,      /* workspace or blockmap buffer too small */
+  TREE_ERR_BOUNDS = 9          /* an index read from device memory points outside the buffer
+                                  it addresses (device-detected; TREE_DEBUG builds) */
 } tree_status_t;
 
 /* Human-readable name of a status code (static string). */
@@ -84,6 +86,24 @@ TREE_API const char* tree_status_string(int status);
 
 /* Library version as "major.minor.patch". */
 TREE_API const char* tree_version(void);
+
+/* ------------------------------------------------------------------------
+ * tree_debug_build — 1 for the bounds-checked TREE_DEBUG build, else 0.
+ *
+ * The library is built twice from the same sources: libtreeattn.so, and
+ * libtreeattn_debug.so compiled with TREE_DEBUG.  Indices that a kernel
+ * computes from its launch shape and the sizes passed to the call are in
+ * range by construction in both.  The debug build also checks, before use,
+ * every index a kernel reads from device memory — the blockmap's row order,
+ * row offsets, counts and key-block lists, its column order, and key_reach
+ * values — against the buffer it addresses.  A failed check writes
+ * TREE_ERR_BOUNDS to *dev_status and the work that depends on it is
+ * skipped (the CTA returns before its first dependent access); nothing
+ * traps or asserts, so the context stays usable.  The release build
+ * trusts those buffers to come from tree_pack_positions and
+ * tree_blockmap_build.
+ * ---------------------------------------------------------------------- */
+TREE_API int32_t tree_debug_build(void);
 
 /* ------------------------------------------------------------------------
  * tree_pack_positions — per-key reach and position ids.

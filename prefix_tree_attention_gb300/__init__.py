@@ -23,11 +23,15 @@ from dataclasses import dataclass
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "lib", "libtreeattn.so")
+# PREFIX_TREE_ATTN_DEBUG=1 selects the bounds-checked TREE_DEBUG build of the
+# same sources (``build.py --debug``); the entry points are the same.
+_DEBUG = os.environ.get("PREFIX_TREE_ATTN_DEBUG", "0") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "lib", "libtreeattn_debug.so" if _DEBUG else "libtreeattn.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python prefix_tree_attention_gb300/build.py`")
+        f"{LIB_PATH} is missing: build it with `python prefix_tree_attention_gb300/build.py"
+        + (" --debug`" if _DEBUG else "`"))
 
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -36,6 +40,7 @@ _P, _I32, _I64, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ct
 _sig = {
     "tree_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tree_version": (ctypes.c_char_p, []),
+    "tree_debug_build": (_I32, []),
     "tree_pack_positions_workspace_bytes": (_SZ, [_I32, _I32]),
     "tree_pack_positions": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _P, _P, _P, _SZ, _P, _P]),
     "tree_blockmap_bytes": (_SZ, [_I32]),
@@ -97,6 +102,11 @@ def status_string(status: int) -> str:
 
 def version() -> str:
     return _lib.tree_version().decode()
+
+
+def debug_build() -> bool:
+    """True when the loaded library is the bounds-checked TREE_DEBUG build."""
+    return bool(_lib.tree_debug_build())
 
 
 def _check(fn: str, status: int) -> None:

@@ -19,6 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "lib")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libtreeattn.so"
+DEBUG_LIB_NAME = "libtreeattn_debug.so"     # the same sources with TREE_DEBUG
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 CUDA_SOURCES = ["api.cu", "positions.cu", "blockmap.cu", "attn_fwd.cu", "attn_bwd.cu",
@@ -38,23 +39,28 @@ def _run(cmd):
     return r.stdout + r.stderr
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every source and link the shared library; returns its path."""
+def build(verbose: bool = False, ptxas_info: bool = False, debug: bool = False) -> str:
+    """Compile every source and link the shared library; returns its path.
+    ``debug`` builds the bounds-checked variant (``-DTREE_DEBUG``) as
+    ``libtreeattn_debug.so`` next to the release library."""
+    build_dir = BUILD_DIR + ("_debug" if debug else "")
     os.makedirs(OUT_DIR, exist_ok=True)
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     cuda_flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                          "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr"]
+    if debug:
+        cuda_flags += ["-DTREE_DEBUG"]
     if ptxas_info:
         cuda_flags += ["-Xptxas", "-v"]
     jobs = []
     objs = []
     for src in CUDA_SOURCES:
-        obj = os.path.join(BUILD_DIR, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         objs.append(obj)
         jobs.append([nvcc] + cuda_flags + ["-c", os.path.join(CSRC, src), "-o", obj])
     for src in CXX_SOURCES:
-        obj = os.path.join(BUILD_DIR, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         objs.append(obj)
         jobs.append([nvcc, "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",
                      "-fvisibility=hidden", "-c", os.path.join(CSRC, src), "-o", obj])
@@ -64,7 +70,7 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
         for log in logs:
             if log.strip():
                 print(log)
-    out = os.path.join(OUT_DIR, LIB_NAME)
+    out = os.path.join(OUT_DIR, DEBUG_LIB_NAME if debug else LIB_NAME)
     tmp = out + ".tmp"
     _run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs)
     os.replace(tmp, out)
@@ -72,5 +78,5 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
 
 
 if __name__ == "__main__":
-    path = build(verbose=True, ptxas_info="--ptxas" in sys.argv)
+    path = build(verbose=True, ptxas_info="--ptxas" in sys.argv, debug="--debug" in sys.argv)
     print(path)

@@ -136,11 +136,14 @@ const char* tree_status_string(int status) {
     case TREE_ERR_CUDA: return "TREE_ERR_CUDA";
     case TREE_ERR_TIMEOUT: return "TREE_ERR_TIMEOUT";
     case TREE_ERR_WORKSPACE: return "TREE_ERR_WORKSPACE";
+    case TREE_ERR_BOUNDS: return "TREE_ERR_BOUNDS";
     default: return "TREE_ERR_UNKNOWN";
   }
 }
 
 const char* tree_version(void) { return "0.1.0"; }
+
+int32_t tree_debug_build(void) { return tree::kDebugBuild ? 1 : 0; }
 
 size_t tree_pack_positions_workspace_bytes(int32_t T_pad, int32_t n_nodes) {
   if (T_pad < 0 || n_nodes < 0) return 0;

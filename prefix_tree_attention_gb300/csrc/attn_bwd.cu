@@ -174,6 +174,7 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     rank = heavy_n + j % nl;
   }
   const int32_t kb = bm.col_order()[rank];
+  if (!dcheck(kb >= 0 && kb < p.nb, p.status)) return;    // CTA-uniform, before TMEM
   const int32_t col_full_hi = bm.col_full_hi()[kb];
   // the key block's column run kb..col_hi, clipped to the window's blocks
   const int32_t qa_first = max(kb, p.row_lo / kBlock);

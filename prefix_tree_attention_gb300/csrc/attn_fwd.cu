@@ -284,12 +284,30 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int32_t unit = blockIdx.x / (gpk * p.n_qa);
   const int32_t j = blockIdx.x % (gpk * p.n_qa);
   const int32_t qa = p.windowed ? p.qa_lo + j / gpk : bm.row_order()[j / gpk];
+  if (!dcheck(qa >= 0 && qa < p.nb, p.status)) return;
   const int32_t h0 = (unit * gpk + j % gpk) * p.heads_per_cta;
   const int nh = p.heads_per_cta;
   const int32_t kvh = h0 / (p.Hq / p.Hkv);
   const int32_t ntiles = bm.row_cnt()[qa];
   const int32_t nfull = bm.row_nfull()[qa];
-  const int32_t* tiles = bm.row_idx() + bm.row_ptr()[qa];
+  const int32_t row_off = bm.row_ptr()[qa];
+  const int32_t* tiles = bm.row_idx() + row_off;
+  if constexpr (kDebugBuild) {
+    // The row's list must lie inside the CSR array (nb (nb + 1) / 2 words),
+    // hold at most qa + 1 key blocks, FULL ones first, each in [0, qa].
+    const int64_t cap = static_cast<int64_t>(p.nb) * (p.nb + 1) / 2;
+    if (!dcheck(row_off >= 0 && ntiles >= 0 && ntiles <= qa + 1 &&
+                    row_off + static_cast<int64_t>(ntiles) <= cap && nfull >= 0 &&
+                    nfull <= ntiles,
+                p.status))
+      return;
+    bool bad = false;
+    for (int32_t k = threadIdx.x; k < ntiles; k += blockDim.x) bad |= tiles[k] < 0 || tiles[k] > qa;
+    if (__syncthreads_or(bad)) {
+      dcheck(false, p.status);
+      return;
+    }
+  }
   AbortState ab{&sm.abort_flag, p.status};
 
   if (threadIdx.x == 0) {

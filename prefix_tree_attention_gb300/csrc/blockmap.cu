@@ -26,7 +26,7 @@ namespace {
 
 constexpr int kWarpsPerCta = 8;
 
-__global__ void k_cols(const int32_t* reach, BlockmapView bm, const int32_t* status) {
+__global__ void k_cols(const int32_t* reach, BlockmapView bm, int32_t* status) {
   if (ld_status(status)) return;
   const int32_t kb = blockIdx.x * kWarpsPerCta + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
@@ -36,6 +36,8 @@ __global__ void k_cols(const int32_t* reach, BlockmapView bm, const int32_t* sta
   for (int t = 0; t < kBlock / 32; ++t) {
     int32_t j = kb * kBlock + t * 32 + lane;
     int32_t r = reach[j];
+    // a key's reach lies in [j - 1, T_pad - 1] (j - 1 for a pad)
+    if constexpr (kDebugBuild) dcheck(r >= j - 1 && r < bm.nb * kBlock, status);
     mn = min(mn, r);
     mx = max(mx, r);
     real |= (r >= j);

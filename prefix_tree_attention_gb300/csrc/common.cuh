@@ -36,6 +36,23 @@ __device__ __forceinline__ int ld_status(const int32_t* s) {
 }
 __device__ __forceinline__ void set_status(int32_t* s, int code) { atomicCAS(s, 0, code); }
 
+// TREE_DEBUG builds check every index read from device memory before it is
+// used (see tree_debug_build).  dcheck(ok, status) is true in a release
+// build; in a debug build it records TREE_ERR_BOUNDS when ok is false.
+#ifdef TREE_DEBUG
+constexpr bool kDebugBuild = true;
+#else
+constexpr bool kDebugBuild = false;
+#endif
+__device__ __forceinline__ bool dcheck(bool ok, int32_t* status) {
+  if constexpr (kDebugBuild) {
+    if (!ok) set_status(status, TREE_ERR_BOUNDS);
+    return ok;
+  } else {
+    return true;
+  }
+}
+
 // Number of kernels this library has launched in the process (all entry
 // points); every launcher adds the launches it queues.
 void count_launches(int n);

@@ -34,10 +34,25 @@ def test_every_declared_symbol_is_exported():
     assert set(ptg.EXPORTED_SYMBOLS) == set(names)
 
 
+
+def test_debug_build_exports_the_same_symbols():
+    dbg = os.path.join(os.path.dirname(ptg.LIB_PATH), "libtreeattn_debug.so")
+    if not os.path.exists(dbg):
+        pytest.skip("the TREE_DEBUG library is not built")
+    d = ctypes.CDLL(dbg)
+    for n in _declared_functions():
+        assert hasattr(d, n), f"{n} declared but not exported by the debug build"
+    d.tree_debug_build.restype = ctypes.c_int32
+    lib.tree_debug_build.restype = ctypes.c_int32
+    assert d.tree_debug_build() == 1 and lib.tree_debug_build() == 0
+    d.tree_status_string.restype = ctypes.c_char_p
+    assert d.tree_status_string(9) == b"TREE_ERR_BOUNDS"
+
 def test_status_strings_and_version():
     assert ptg.status_string(0) == "TREE_OK"
     assert ptg.status_string(4) == "TREE_ERR_MALFORMED_TREE"
     assert ptg.status_string(7) == "TREE_ERR_TIMEOUT"
+    assert ptg.status_string(9) == "TREE_ERR_BOUNDS"
     assert ptg.status_string(99) == "TREE_ERR_UNKNOWN"
     assert re.fullmatch(r"\d+\.\d+\.\d+", ptg.version())
 

@@ -461,6 +461,52 @@ TREE_API tree_status_t tree_merge_per_sequence(const float* src, int64_t n_src,
                                                int32_t* dev_status, tree_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * tree_lm_head_logprobs_entropy — the LM head fused with the gather.
+ *
+ * Source: the guide's section "Log Probability 计算：树结构的特殊处理": the
+ * log-probabilities and entropies of a packed tree are taken chunk by chunk
+ * so that the [tokens, vocabulary] logits are never held at once.  Here the
+ * logits logits[r, v] = sum_k hidden[r, k] * weight[v, k] (fp32 sums of bf16
+ * products) exist only one 128 x 256 tile at a time, in tensor memory, and
+ * the outputs are those of tree_logprobs_entropy on them:
+ *     lse[r], entropy[r], vocab_min[r], vocab_max[r]   per real row
+ *     logprob[j] = logits[pred(j), token_ids[j]] - lse[pred(j)],  token_pred[j]
+ * with pred(j) as there (pads: 0 and -1).  The label logit is recomputed
+ * as a fp32 dot product, so its rounding differs from the tile's by the
+ * order of the sum.
+ *
+ *   hidden        [in]  device bf16 [T_pad, H] row-major, 16-byte aligned
+ *   weight        [in]  device bf16 [V, H] row-major (one row per vocabulary
+ *                       entry: the LM head / tied embedding), 16-byte aligned
+ *   H             hidden size, a multiple of 64 (else TREE_ERR_UNSUPPORTED)
+ *   token_ids, key_reach, blockmap, blockmap_bytes, lse, entropy, vocab_min,
+ *   vocab_max, logprob, token_pred   as in tree_logprobs_entropy
+ *   workspace     [scratch] device, 16-byte aligned,
+ *                 >= tree_lm_head_workspace_bytes(T_pad, V) bytes (per-row
+ *                 partial statistics of every 2048-column vocabulary chunk)
+ *   dev_status    [out] TREE_ERR_MALFORMED_TREE for a label id outside [0, V);
+ *                 TREE_ERR_TIMEOUT if a device wait ran out of time
+ * Returns TREE_ERR_INVALID_ARG for a missing required pointer, H < 1 or
+ * V < 1, TREE_ERR_ALIGNMENT for T_pad % 128 != 0 or an unaligned buffer,
+ * TREE_ERR_WORKSPACE for a short workspace or blockmap.  T_pad == 0 is a
+ * no-op.  Three launches: the persistent tcgen05 GEMM with the row
+ * statistics in its epilogue (one CTA per SM), the combination of the
+ * partials, and the labels (skipped when neither logprob nor token_pred is
+ * requested).
+ * ---------------------------------------------------------------------- */
+TREE_API size_t tree_lm_head_workspace_bytes(int32_t T_pad, int32_t V);
+TREE_API tree_status_t tree_lm_head_logprobs_entropy(const void* hidden, const void* weight,
+                                                     int32_t T_pad, int32_t H, int32_t V,
+                                                     const int32_t* token_ids,
+                                                     const int32_t* key_reach,
+                                                     const void* blockmap, size_t blockmap_bytes,
+                                                     float* lse, float* entropy,
+                                                     float* vocab_min, float* vocab_max,
+                                                     float* logprob, int32_t* token_pred,
+                                                     void* workspace, size_t workspace_bytes,
+                                                     int32_t* dev_status, tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * tree_merge_per_sequence_bwd — the merge's adjoint (its gradient).
  *
  * Source: the same section; the page's merge is part of a differentiable

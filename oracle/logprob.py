@@ -48,7 +48,10 @@ backward (``gather_packed_tree_backward``, the gradient a training step takes
 through the gather) is pinned by float64 torch autograd through the
 per-sequence computation on the unpacked rows, by central differences of the
 forward on tiny tries, and by closed forms (uniform rows; rows of the
-gradient sum to zero).  See tests/test_oracle_logprob.py.
+gradient sum to zero).  ``lm_head_logits`` is pinned by weights whose
+products are known exactly (the identity and a permutation give the hidden
+states themselves, a rank-one pair gives H a b^T).  See
+tests/test_oracle_logprob.py.
 """
 from __future__ import annotations
 
@@ -223,6 +226,15 @@ def combine_vocab_slices(stats) -> tuple[float, float, float, float]:
     w = np.exp(lses - lse)
     ent = float((w * (np.array([s[1] for s in stats]) + lse - lses)).sum())
     return float(lse), ent, float(min(s[2] for s in stats)), float(max(s[3] for s in stats))
+
+
+def lm_head_logits(hidden, weight) -> np.ndarray:
+    """The LM head that produces the gather's input: logits[r, v] =
+    sum_k hidden[r, k] * weight[v, k] (one weight row per vocabulary entry),
+    float64.  The same section's gather then runs on these logits; its
+    chunking changes no value, so the oracle takes them whole (or for a
+    subset of rows, ``hidden[rows]``)."""
+    return np.asarray(hidden, dtype=np.float64) @ np.asarray(weight, dtype=np.float64).T
 
 
 def sequence_pairs(packed, sid: int) -> list[tuple[int, int]]:

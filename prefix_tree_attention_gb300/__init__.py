@@ -11,6 +11,7 @@ tensors, checks their dtype/shape/device, passes raw pointers and the current
 CUDA stream, and raises ``TreeError`` on a non-OK status), the log-probability
 gather ``tree_logprobs_entropy`` with its merge ``tree_merge_per_sequence``
 and their gradients ``tree_logprobs_entropy_bwd`` / ``tree_merge_per_sequence_bwd``,
+the LM head fused with the gather ``tree_lm_head_logprobs_entropy``,
 plus the host packer ``pack_sequences``, partitioner ``partition_sequences``
 and the DFS traversal schedule ``dta_schedule``.
 """
@@ -72,6 +73,9 @@ _sig = {
                                                    _I64, _P, _P]),
     "tree_logprobs_entropy_bwd": (ctypes.c_int, [_P, _I32, _I64, _I32, _I32, _P, _P, _P, _P, _P,
                                                  _P, _P, _I64, _P, _P]),
+    "tree_lm_head_workspace_bytes": (_SZ, [_I32, _I32]),
+    "tree_lm_head_logprobs_entropy": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _SZ,
+                                                     _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tree_dta_schedule": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _P]),
     "tree_dta_attn_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32]),
     "tree_dta_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _SZ, _I32, _I32, _I32, _I32, _F32,
@@ -371,6 +375,44 @@ def tree_logprobs_entropy_bwd(logits, key_reach, lse, grad_logits, dev_status, t
         _ptr(logits), code, logits.stride(0), T_pad, V, _ptr(token_ids), _ptr(key_reach),
         _ptr(lse), _ptr(entropy), _ptr(grad_logprob), _ptr(grad_entropy), _ptr(grad_logits),
         grad_logits.stride(0), _ptr(dev_status), _stream_ptr(stream)))
+
+
+def lm_head_workspace_bytes(T_pad: int, V: int) -> int:
+    return int(_lib.tree_lm_head_workspace_bytes(int(T_pad), int(V)))
+
+
+def tree_lm_head_logprobs_entropy(hidden, weight, key_reach, lse, workspace, dev_status,
+                                  token_ids=None, blockmap=None, entropy=None, vocab_min=None,
+                                  vocab_max=None, logprob=None, token_pred=None, stream=None):
+    """The LM head (``hidden [T_pad, H] @ weight [V, H]^T``, bf16) fused with
+    the gather: the outputs of ``tree_logprobs_entropy`` without the logits
+    ever being written."""
+    import torch
+    _on_device(hidden=hidden, weight=weight, key_reach=key_reach, lse=lse, workspace=workspace,
+               dev_status=dev_status, token_ids=token_ids, blockmap=blockmap, entropy=entropy,
+               vocab_min=vocab_min, vocab_max=vocab_max, logprob=logprob, token_pred=token_pred)
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight, torch.bfloat16, "weight")
+    if hidden.dim() != 2 or weight.dim() != 2 or hidden.shape[1] != weight.shape[1]:
+        raise ValueError("hidden must be [T_pad, H] and weight [V, H]")
+    T_pad, H = hidden.shape
+    V = weight.shape[0]
+    _need(key_reach, torch.int32, "key_reach")
+    if blockmap is not None:
+        _need(blockmap, torch.int32, "blockmap")
+    for t, n in ((key_reach, "key_reach"), (token_ids, "token_ids"), (token_pred, "token_pred"),
+                 (lse, "lse"), (entropy, "entropy"), (vocab_min, "vocab_min"),
+                 (vocab_max, "vocab_max"), (logprob, "logprob")):
+        if t is not None:
+            _need(t, torch.int32 if n in ("key_reach", "token_ids", "token_pred")
+                  else torch.float32, n)
+            if t.numel() != T_pad:
+                raise ValueError(f"{n} must hold T_pad = {T_pad} values")
+    _check("tree_lm_head_logprobs_entropy", _lib.tree_lm_head_logprobs_entropy(
+        _ptr(hidden), _ptr(weight), T_pad, H, V, _ptr(token_ids), _ptr(key_reach),
+        _ptr(blockmap), 0 if blockmap is None else _nbytes(blockmap), _ptr(lse), _ptr(entropy),
+        _ptr(vocab_min), _ptr(vocab_max), _ptr(logprob), _ptr(token_pred), _ptr(workspace),
+        _nbytes(workspace), _ptr(dev_status), _stream_ptr(stream)))
 
 
 DTA_FWD_PUSH, DTA_FWD_BWD, DTA_BWD_POP = 0, 1, 2

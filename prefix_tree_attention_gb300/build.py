@@ -23,7 +23,7 @@ DEBUG_LIB_NAME = "libtreeattn_debug.so"     # the same sources with TREE_DEBUG
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 CUDA_SOURCES = ["api.cu", "positions.cu", "blockmap.cu", "attn_fwd.cu", "attn_bwd.cu",
-                "diag.cu", "logprob.cu", "dta_attn.cu"]
+                "diag.cu", "logprob.cu", "dta_attn.cu", "lmhead.cu"]
 CXX_SOURCES = ["packer.cpp", "partition.cpp", "dta.cpp"]
 
 

@@ -37,6 +37,13 @@ cudaError_t launch_dta_init(void* o, void* dq, float* lse, void* workspace, size
 cudaError_t launch_dta_finish(const float* dk_acc, const float* dv_acc, void* dk, void* dv,
                               int32_t T_pad, int32_t Hkv, int32_t d, int32_t* status,
                               cudaStream_t s, int num_sms);
+size_t lm_head_workspace_bytes(int32_t T_pad, int32_t V);
+cudaError_t launch_lm_head(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const void* hidden,
+                           const void* weight, int32_t T_pad, int32_t H, int32_t V,
+                           const int32_t* token_ids, const int32_t* key_reach,
+                           const void* blockmap, float* lse, float* entropy, float* vmin,
+                           float* vmax, float* logprob, int32_t* token_pred, void* workspace,
+                           int32_t* status, cudaStream_t s, int num_sms);
 
 namespace {
 std::atomic<uint64_t> g_launches{0};
@@ -101,6 +108,22 @@ bool encode_map_acc(CUtensorMap* map, void* base, int32_t T, int32_t H, int32_t 
   if (!fn) return false;
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, elem,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// A row-major [rows, cols] bf16 matrix as a 2-D TMA map with a 64-column
+// (128-byte) x box_rows box, 128-byte swizzle; rows past the end read as 0.
+bool encode_map_2d(CUtensorMap* map, const void* base, int64_t rows, int32_t cols,
+                   uint32_t box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t elem[2] = {1, 1};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                  strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -375,5 +398,41 @@ tree_status_t tree_dta_attn(const void* q, const void* k, const void* v, const v
 }
 
 uint64_t tree_launch_count(void) { return tree::launches_total(); }
+
+size_t tree_lm_head_workspace_bytes(int32_t T_pad, int32_t V) {
+  if (T_pad < 0 || V < 1) return 0;
+  return tree::lm_head_workspace_bytes(T_pad, V);
+}
+
+tree_status_t tree_lm_head_logprobs_entropy(const void* hidden, const void* weight,
+                                            int32_t T_pad, int32_t H, int32_t V,
+                                            const int32_t* token_ids, const int32_t* key_reach,
+                                            const void* blockmap, size_t blockmap_bytes,
+                                            float* lse, float* entropy, float* vocab_min,
+                                            float* vocab_max, float* logprob,
+                                            int32_t* token_pred, void* workspace,
+                                            size_t workspace_bytes, int32_t* dev_status,
+                                            tree_stream_t stream) {
+  if (T_pad < 0 || H < 1 || V < 1 || !dev_status) return TREE_ERR_INVALID_ARG;
+  if (T_pad % tree::kBlock) return TREE_ERR_ALIGNMENT;
+  if (H % 64) return TREE_ERR_UNSUPPORTED;
+  if (T_pad == 0) return TREE_OK;
+  if (!hidden || !weight || !key_reach || !lse || !workspace) return TREE_ERR_INVALID_ARG;
+  const bool labels = logprob != nullptr || token_pred != nullptr;
+  if (labels && !blockmap) return TREE_ERR_INVALID_ARG;
+  if (logprob && !token_ids) return TREE_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(workspace))
+    return TREE_ERR_ALIGNMENT;
+  if (labels && blockmap_bytes < tree_blockmap_bytes(T_pad)) return TREE_ERR_WORKSPACE;
+  if (workspace_bytes < tree::lm_head_workspace_bytes(T_pad, V)) return TREE_ERR_WORKSPACE;
+  CUtensorMap th, tw;
+  if (!encode_map_2d(&th, hidden, T_pad, H, 128) || !encode_map_2d(&tw, weight, V, H, 256))
+    return TREE_ERR_CUDA;
+  return cuda_result(tree::launch_lm_head(th, tw, hidden, weight, T_pad, H, V, token_ids,
+                                          key_reach, blockmap, lse, entropy, vocab_min,
+                                          vocab_max, logprob, token_pred, workspace, dev_status,
+                                          reinterpret_cast<cudaStream_t>(stream),
+                                          num_sms_current()));
+}
 
 }  // extern "C"

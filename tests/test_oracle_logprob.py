@@ -338,3 +338,28 @@ def test_merge_backward_is_the_adjoint():
         lhs = float((lin * g).sum())
         rhs = sum(float(np.dot(part[s], bp[s])) for part, bp in zip(res, back) for s in part)
         assert abs(lhs - rhs) < 1e-12
+
+
+
+# ------------------------------------------------------------------ LM head
+def test_lm_head_logits_exact_products():
+    rng = np.random.default_rng(3)
+    hidden = rng.standard_normal((37, 16))
+    # the identity: logits are the hidden states themselves
+    np.testing.assert_array_equal(OL.lm_head_logits(hidden, np.eye(16)), hidden)
+    # a permutation of vocabulary rows permutes the logits' columns
+    perm = rng.permutation(16)
+    np.testing.assert_array_equal(OL.lm_head_logits(hidden, np.eye(16)[perm]), hidden[:, perm])
+    # rank one: hidden = a 1^T, weight = b 1^T gives H a b^T (small integers: exact)
+    a, b = rng.integers(-8, 9, 37).astype(float), rng.integers(-8, 9, 11).astype(float)
+    got = OL.lm_head_logits(np.outer(a, np.ones(16)), np.outer(b, np.ones(16)))
+    np.testing.assert_array_equal(got, 16 * np.outer(a, b))
+    # the gather on LM-head logits of identity weights is the gather on the
+    # hidden states
+    seqs = [[1, 2, 3, 4], [1, 2, 5], [6, 7]]
+    (t,) = OT.pack_sequences(seqs, 128)
+    h = rng.standard_normal((t.T_pad, 16))
+    r1, _ = OL.gather_packed_tree_logprobs_entropy(OL.lm_head_logits(h, np.eye(16)), t)
+    r2, _ = OL.gather_packed_tree_logprobs_entropy(h, t)
+    for sid in t.seq_ids:
+        np.testing.assert_array_equal(r1[sid][0], r2[sid][0])

@@ -201,3 +201,17 @@ def logits(T: int, V: int, seed: int, device="cpu", dtype=None, sigma: float = 2
     buf = torch.randn((T, width), generator=g, device=device, dtype=torch.float32)
     buf = (buf * sigma).to(dtype)
     return buf[:, :V]
+
+
+def lm_head(T: int, H: int, V: int, seed: int, device="cpu"):
+    """Hidden states [T, H] ~ N(0, 1) and LM-head weights [V, H] ~
+    N(0, (2 / sqrt(H))^2), both rounded to bf16, so the logits
+    hidden @ weight^T have standard deviation about 2 (the sigma of
+    ``logits``)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed((0x1A4E + 7919 * seed) & ((1 << 63) - 1))
+    hidden = torch.randn((T, H), generator=g, device=device, dtype=torch.float32)
+    weight = torch.randn((V, H), generator=g, device=device, dtype=torch.float32)
+    weight *= 2.0 / float(H) ** 0.5
+    return hidden.to(torch.bfloat16), weight.to(torch.bfloat16)

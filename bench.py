@@ -15,11 +15,12 @@ visible pairs count only unmasked (i, j) over real tokens (4 d Hq per pair
 for the forward, 10 d Hq for the backward).  Packed tokens/s is reported too.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--split replicas|balanced] [--path attention|logprob|dta]
+                       [--split replicas|balanced] [--path attention|logprob|dta|lmhead]
 --path logprob times the tree-aware log-probability / entropy gather over the
 same batch instead (bf16 logits over the Qwen3 vocabulary; its own JSON line);
 --path dta runs the attention through the depth-first traversal schedule of
-dynamic tree attention (--chunk tokens per op) beside the packed step.
+dynamic tree attention (--chunk tokens per op) beside the packed step;
+--path lmhead times Qwen3-8B's LM head fused with the gather (no logits).
 Under torchrun each rank runs its own batch (seed = rank, --split replicas,
 the default): weak scaling, no collective on the data path.  With --split
 balanced every rank takes the same global batch and keeps one group of the
@@ -292,11 +293,37 @@ def run_reference_logprob(args):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_lmhead(args):
+    budget = min(args.cpu_budget, 15.0)
+    vals, desc = [], None
+    for step in range(args.warmup + args.steps):
+        v, desc = lmhead_oracle_rate(budget / max(1, args.warmup + args.steps) * 4, args.seed)
+        if step >= args.warmup:
+            vals.append(v)
+    value = round(float(np.median(vals)), 3)
+    line = {
+        "impl": "reference", "metric": LMHEAD_METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "path": "lmhead", "hidden": QWEN3_HIDDEN,
+                   "vocab": QWEN3_VOCAB},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, rank, ws):
     if rank != 0:
         return
     if args.path == "logprob":
         run_reference_logprob(args)
+        return
+    if args.path == "lmhead":
+        run_reference_lmhead(args)
         return
     budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
     vals = []
@@ -955,6 +982,195 @@ def logprob_backward(ptg, cases, offs, logits, lse_all, ent_all, pos_d, soffs_d,
     }
 
 
+LMHEAD_METRIC = "LM head fused with the tree log-prob gather, packed tokens/s"
+QWEN3_HIDDEN = 4096
+
+
+def lmhead_oracle_child(budget_s: float, seed: int, rows: int, H: int, V: int, v_slice: int):
+    """Body of the oracle timing for ``--path lmhead`` (run in a child process
+    whose BLAS is limited to one thread): per pass, the LM-head logits of
+    ``rows`` token rows against a ``v_slice``-row slice of the weights in
+    fp64 (``oracle.logprob.lm_head_logits``), then each row's statistics and
+    log-softmax over the slice; rows per second are scaled by v_slice / V to
+    the whole vocabulary.  Prints one JSON object."""
+    from oracle import logprob as OL
+    hidden, weight = W.lm_head(rows, H, v_slice, seed=seed)
+    h = hidden.float().numpy().astype(np.float64)
+    w = weight.float().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        x = OL.lm_head_logits(h, w)
+        for r in range(rows):
+            OL.row_stats(x[r])
+            OL.log_softmax(x[r])
+        passes += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    rate = passes * rows / dt * v_slice / V
+    print(json.dumps({"rate": rate, "sample": (
+        f"{passes} passes of {rows} rows x H={H} against a {v_slice}-row vocabulary slice "
+        f"(fp64 numpy LM-head logits + row stats + log-softmax, one BLAS thread), "
+        f"scaled to V={V}")}))
+
+
+def lmhead_oracle_rate(budget_s: float, seed: int, rows: int = 16, H: int = QWEN3_HIDDEN,
+                       V: int = QWEN3_VOCAB, v_slice: int = 16384):
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import bench; bench.lmhead_oracle_child(%r, %d, %d, %d, %d, %d)"
+            % (budget_s, seed, rows, H, V, v_slice))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
+    rec = json.loads(r.stdout.strip().splitlines()[-1])
+    return rec["rate"], rec["sample"]
+
+
+def run_lmhead(args, rank, ws):
+    """``--path lmhead``: the LM head fused with the log-prob gather.
+
+    One step = for every trie of the batch, tree_lm_head_logprobs_entropy
+    over that trie's rows: Qwen3-8B's LM head (hidden size 4096, vocabulary
+    151,936, bf16 hidden states [T_pad, 4096] and weights [151936, 4096],
+    synthetic N(0, 1) and N(0, (2/64)^2)) with the row log-sum-exp and
+    entropy in the GEMM's epilogue and each token's label log-probability;
+    then the merge of log-probabilities and entropies into [n_seqs, max_len].
+    Positions and blockmap (a1, a2) are inputs here.  No logits buffer
+    exists.  The roofline is the call's GEMM against the bf16 tensor peak:
+    2 * real rows * V * H flops per trie."""
+    import torch
+    import prefix_tree_attention_gb300 as ptg
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    wl = W.WORKLOADS[args.workload]
+    seqs, seed = rank_batch(ptg, args.workload, args.seed, rank, ws, args.split)
+    tries = ptg.pack_sequences(seqs, wl.max_tokens_per_mb)
+    if args.tries:
+        tries = tries[:args.tries]
+    used = sorted({s for tr in tries for s in tr.seq_ids})
+    remap = {s: i for i, s in enumerate(used)}
+    for tr in tries:
+        tr.seq_index = {remap[s]: v for s, v in tr.seq_index.items()}
+    V, H = QWEN3_VOCAB, QWEN3_HIDDEN
+    t_max = max(tr.T_pad for tr in tries)
+    hidden, weight = W.lm_head(t_max, H, V, seed=seed, device=device)
+    offs = np.cumsum([0] + [tr.T_pad for tr in tries]).tolist()
+    total = offs[-1]
+    f32 = dict(dtype=torch.float32, device=device)
+    lse_all, ent_all, lp_all = (torch.empty(total, **f32) for _ in range(3))
+    ws_buf = torch.empty(ptg.lm_head_workspace_bytes(t_max, V) // 4, **f32)
+    cases = []
+    for tr in tries:
+        bufs = ptg.TrieBuffers(tr.T_pad, tr.n_nodes, 1, 64, device=device)
+        ptg.tree_pack_positions(torch.from_numpy(tr.token_node).to(device),
+                                torch.from_numpy(tr.node_entry).to(device),
+                                torch.from_numpy(tr.node_exit).to(device), bufs.position_ids,
+                                bufs.key_reach, bufs.pos_ws, bufs.status)
+        ptg.tree_blockmap_build(bufs.key_reach, bufs.blockmap, bufs.status)
+        tok = np.where(tr.token_ids >= 0, tr.token_ids % V, -1).astype(np.int32)
+        cases.append((tr, bufs, torch.from_numpy(tok).to(device)))
+    pos, soffs = ptg.sequence_index_arrays(tries, len(used), offs[:-1])
+    pos_d = torch.from_numpy(pos).to(device)
+    soffs_d = torch.from_numpy(soffs).to(device)
+    max_len = max(int(soffs[i + 1] - soffs[i]) for i in range(len(used))) - 1
+    out_lp = torch.empty((len(used), max_len), **f32)
+    out_ent = torch.empty_like(out_lp)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+    tokens = sum(tr.n_tokens for tr in tries)
+
+    def call(i, tr, bufs, tok, labels=True):
+        sl = slice(offs[i], offs[i + 1])
+        ptg.tree_lm_head_logprobs_entropy(
+            hidden[:tr.T_pad], weight, bufs.key_reach, lse_all[sl], ws_buf, bufs.status,
+            token_ids=tok, blockmap=bufs.blockmap, entropy=ent_all[sl],
+            logprob=lp_all[sl] if labels else None)
+
+    def step():
+        for i, (tr, bufs, tok) in enumerate(cases):
+            call(i, tr, bufs, tok)
+        ptg.tree_merge_per_sequence(lp_all, pos_d, soffs_d, out_lp, status, 1, 1, 0.0)
+        ptg.tree_merge_per_sequence(ent_all, pos_d, soffs_d, out_ent, status, 0, 1, 0.0)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bad = [int(b.status.item()) for _, b, _ in cases] + [int(status.item())]
+    if any(bad):
+        raise RuntimeError("device status " + ptg.status_string(max(bad)))
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    launches0 = ptg.launch_count()
+    barrier(ws)
+    torch.cuda.synchronize()
+    per_step = []
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            s0, s1 = mk(), mk()
+            s0.record(stream)
+            step()
+            s1.record(stream)
+            per_step.append((s0, s1))
+        torch.cuda.synchronize()
+    barrier(ws)
+    launches = ptg.launch_count() - launches0
+    ms_per_step = float(np.mean([a.elapsed_time(b) for a, b in per_step]))
+    ms_max = max_over_ranks(ms_per_step, ws)
+    tokens_all = sum_over_ranks(tokens, ws)
+    # the GEMM with its statistics epilogue and the partials' combine, each
+    # call bracketed by events (the label pass left out)
+    gemm_ms = 0.0
+    for i, (tr, bufs, tok) in enumerate(cases):
+        e0, e1 = mk(), mk()
+        e0.record(stream)
+        call(i, tr, bufs, tok, labels=False)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        gemm_ms += e0.elapsed_time(e1)
+    flops = sum(2.0 * tr.n_tokens * V * H for tr in tries)
+    peaks = measured_peaks()
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    step_tflops = sum_over_ranks(flops, ws) / (ms_max * 1e-3) / 1e12
+    line = {
+        "metric": LMHEAD_METRIC, "value": round(tokens_all / (ms_max * 1e-3), 1),
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 3), "higher_is_better": True,
+        "scaling": "strong" if (args.split == "balanced" and ws > 1) else "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": args.workload + (f" (first {args.tries} tries)" if args.tries else ""),
+            "path": "lmhead", "tries": len(tries), "packed_tokens": tokens,
+            "sequences": len(used), "hidden": H, "vocab": V,
+            "inputs": "bf16 hidden N(0,1) [T_pad, 4096], weight N(0,(2/64)^2) [151936, 4096]",
+            "step_tflops": round(step_tflops, 1),
+            "l2": "weights (1.24 GB) larger than L2 (no flush needed)",
+            "parallelism": (f"balanced split of one batch x{ws}" if args.split == "balanced"
+                            else f"replicas x{ws}"),
+        },
+        "roofline": {
+            "kernel": "k_lmh_gemm_stats (LM-head GEMM + row statistics) with k_lmh_combine",
+            "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
+            "peak_kind": f"bf16 dense, burst ({peaks['source']})",
+            "frac_of_sustained": round(achieved / peaks["bf16_sustained"], 4),
+            "traffic": None, "avg_launch_ms": round(gemm_ms / len(cases), 4),
+            "flops_per_launch": flops / len(cases),
+        },
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "e2e": None,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, desc = lmhead_oracle_rate(min(args.cpu_budget, 15.0), seed)
+        line["cpu_baseline"] = {"value": round(rate, 3), "unit": "tokens/s", "cores": 1,
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(ptg, cases, ws_bwds, streams, args, ws, flops_all):
     """Same metric, each step copying its inputs host->device from pinned
     memory and its outputs (O, dQ, dK, dV) device->host, through the same
@@ -1111,10 +1327,12 @@ def main(argv=None):
                          "load-balanced partitioner")
     ap.add_argument("--streams", type=int, default=2,
                     help="CUDA streams the independent tries of a batch alternate over")
-    ap.add_argument("--path", choices=["attention", "logprob", "dta"], default="attention",
+    ap.add_argument("--path", choices=["attention", "logprob", "dta", "lmhead"],
+                    default="attention",
                     help="attention: the fwd+bwd step (default); logprob: the tree-aware "
                          "log-prob / entropy gather over packed logits; dta: the same "
-                         "attention executed through the depth-first traversal schedule")
+                         "attention executed through the depth-first traversal schedule; "
+                         "lmhead: the LM head fused with the gather (no logits buffer)")
     ap.add_argument("--chunk", type=int, default=2048,
                     help="--path dta: chunk length of the traversal schedule")
     ap.add_argument("--no-e2e", action="store_true")
@@ -1134,6 +1352,8 @@ def main(argv=None):
         run_logprob(args, rank, ws)
     elif args.path == "dta":
         run_dta(args, rank, ws)
+    elif args.path == "lmhead":
+        run_lmhead(args, rank, ws)
     else:
         run_ours(args, rank, ws)
     if ws > 1:

@@ -43,6 +43,19 @@ def test_reference_arm_logprob_path():
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["config"]["path"] == "logprob"
 
 
+def test_reference_arm_lmhead_path():
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--path", "lmhead", "--steps", "1", "--warmup", "0",
+                    "--cpu-budget", "0.5"])
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.strip()]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["metric"] == bench.LMHEAD_METRIC
+    assert rec["value"] > 0 and rec["cpu_baseline"]["cores"] == 1
+    assert rec["config"]["path"] == "lmhead" and rec["config"]["hidden"] == 4096
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))

@@ -215,6 +215,13 @@ def test_backward_without_transitions_is_caught(monkeypatch):
         TL.test_backward_equals_autograd_of_unpacked_sequences()
 
 
+def test_lm_head_without_transpose_is_caught(monkeypatch):
+    monkeypatch.setattr(OL, "lm_head_logits", lambda hidden, weight: (
+        np.asarray(hidden, dtype=np.float64) @ np.asarray(weight, dtype=np.float64)))
+    with pytest.raises(AssertionError):
+        TL.test_lm_head_logits_exact_products()
+
+
 # ------------------------------------------------------------ DTA schedule
 def test_shallowest_first_order_is_caught(monkeypatch):
     monkeypatch.setattr(OD, "greedy_order", lambda nodes, depth, packed: sorted(

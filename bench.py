@@ -51,10 +51,13 @@ UNIT = "TFLOP/s"
 FWD_FLOPS_PER_PAIR = 4      # times d * Hq
 BWD_FLOPS_PER_PAIR = 10
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "bwd_main_traffic.json")
-KERNEL_SOURCE = os.path.join(ROOT, "prefix_tree_attention_gb300", "csrc", "attn_bwd.cu")
+CSRC = os.path.join(ROOT, "prefix_tree_attention_gb300", "csrc")
+# A kernel's source: its translation unit and the headers it includes.
+KERNEL_SOURCE = [os.path.join(CSRC, f) for f in ("attn_bwd.cu", "common.cuh", "ptx.cuh")]
 LOGPROB_TRAFFIC = os.path.join(ROOT, "profiles", "logprob_row_stats_traffic.json")
 LOGPROB_BWD_TRAFFIC = os.path.join(ROOT, "profiles", "logprob_row_bwd_traffic.json")
-LOGPROB_SOURCE = os.path.join(ROOT, "prefix_tree_attention_gb300", "csrc", "logprob.cu")
+LOGPROB_SOURCE = [os.path.join(CSRC, f)
+                  for f in ("logprob.cu", "rowstats.cuh", "common.cuh", "ptx.cuh")]
 
 
 # ------------------------------------------------------------------ helpers
@@ -81,9 +84,13 @@ def measured_peaks():
     return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
 
 
-def source_hash(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_hash(paths) -> str:
+    """sha256/16 of a kernel's source files, concatenated in the order given."""
+    h = hashlib.sha256()
+    for path in ([paths] if isinstance(paths, str) else paths):
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_logprob_traffic_per_row(path=LOGPROB_TRAFFIC):

@@ -507,6 +507,58 @@ TREE_API tree_status_t tree_lm_head_logprobs_entropy(const void* hidden, const v
                                                      int32_t* dev_status, tree_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * tree_lm_head_logits_grad — gradient of the fused gather w.r.t. the logits,
+ * one chunk of rows at a time, without the logits.
+ *
+ * Source: the same section; the page's gather is differentiated by a
+ * training step and runs chunk by chunk so that the [tokens, vocabulary]
+ * logits are never held at once.  For rows [row_lo, row_hi) this writes
+ *     grad_logits[r - row_lo, v] = sum_{pred(j) = r} grad_logprob[j] * ([v == y_j] - p_v)
+ *                                - grad_entropy[r] * p_v * (logits[r, v] - lse[r] + H)
+ * (the gradient tree_logprobs_entropy_bwd writes from materialised
+ * logits), recomputing each 128 x 256 logits tile hidden W^T in tensor
+ * memory as tree_lm_head_logprobs_entropy does.  The caller then forms the
+ * LM head's own gradients from the chunk with two plain GEMMs:
+ *     d hidden[rows] = grad_logits W,   d W += grad_logits^T hidden[rows].
+ * fp32 arithmetic, one rounding to bf16 per entry; deterministic.
+ *
+ *   hidden, weight, T_pad, H, V, token_ids, key_reach
+ *                 [in]  as in tree_lm_head_logprobs_entropy
+ *   row_lo, row_hi      the chunk: 0 <= row_lo <= row_hi <= T_pad, both
+ *                       multiples of 128 (else TREE_ERR_ALIGNMENT)
+ *   lse, entropy  [in]  device float[T_pad] from tree_lm_head_logprobs_entropy
+ *                       (entropy needed when grad_entropy != NULL)
+ *   grad_logprob  [in]  device float[T_pad] per label token, or NULL
+ *   grad_entropy  [in]  device float[T_pad] per row, or NULL
+ *                       (in the packed layout tree_merge_per_sequence_bwd leaves)
+ *   grad_logits   [out] device bf16 [row_hi - row_lo, grad_row_stride], the
+ *                       first V entries of each row written (pads: 0); rows
+ *                       16-byte aligned (grad_row_stride a multiple of 8)
+ *   workspace     [scratch] device, 16-byte aligned,
+ *                 >= tree_lm_head_grad_workspace_bytes(row_hi - row_lo)
+ *   dev_status    [out] TREE_ERR_MALFORMED_TREE for a child id outside [0, V)
+ *                       (its one-hot term is dropped); TREE_ERR_TIMEOUT
+ * Returns TREE_ERR_INVALID_ARG for a missing required pointer, H < 1,
+ * V < 1, grad_row_stride < V or a chunk outside [0, T_pad),
+ * TREE_ERR_ALIGNMENT, TREE_ERR_UNSUPPORTED for H % 64 != 0,
+ * TREE_ERR_WORKSPACE.  An empty chunk is a no-op.  Three launches (row
+ * coefficients, the GEMM with the gradient epilogue, the one-hot terms;
+ * the last skipped without grad_logprob).
+ * ---------------------------------------------------------------------- */
+TREE_API size_t tree_lm_head_grad_workspace_bytes(int32_t rows);
+TREE_API tree_status_t tree_lm_head_logits_grad(const void* hidden, const void* weight,
+                                                int32_t T_pad, int32_t H, int32_t V,
+                                                int32_t row_lo, int32_t row_hi,
+                                                const int32_t* token_ids,
+                                                const int32_t* key_reach, const float* lse,
+                                                const float* entropy,
+                                                const float* grad_logprob,
+                                                const float* grad_entropy, void* grad_logits,
+                                                int64_t grad_row_stride, void* workspace,
+                                                size_t workspace_bytes, int32_t* dev_status,
+                                                tree_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * tree_merge_per_sequence_bwd — the merge's adjoint (its gradient).
  *
  * Source: the same section; the page's merge is part of a differentiable

@@ -11,7 +11,8 @@ tensors, checks their dtype/shape/device, passes raw pointers and the current
 CUDA stream, and raises ``TreeError`` on a non-OK status), the log-probability
 gather ``tree_logprobs_entropy`` with its merge ``tree_merge_per_sequence``
 and their gradients ``tree_logprobs_entropy_bwd`` / ``tree_merge_per_sequence_bwd``,
-the LM head fused with the gather ``tree_lm_head_logprobs_entropy``,
+the LM head fused with the gather ``tree_lm_head_logprobs_entropy`` and its
+chunked logits gradient ``tree_lm_head_logits_grad``,
 plus the host packer ``pack_sequences``, partitioner ``partition_sequences``
 and the DFS traversal schedule ``dta_schedule``.
 """
@@ -76,6 +77,9 @@ _sig = {
     "tree_lm_head_workspace_bytes": (_SZ, [_I32, _I32]),
     "tree_lm_head_logprobs_entropy": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _P, _P, _P, _SZ,
                                                      _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tree_lm_head_grad_workspace_bytes": (_SZ, [_I32]),
+    "tree_lm_head_logits_grad": (ctypes.c_int, [_P, _P, _I32, _I32, _I32, _I32, _I32, _P, _P,
+                                                _P, _P, _P, _P, _P, _I64, _P, _SZ, _P, _P]),
     "tree_dta_schedule": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _P, _I64, _P, _P]),
     "tree_dta_attn_workspace_bytes": (_SZ, [_I32, _I32, _I32, _I32]),
     "tree_dta_attn": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _SZ, _I32, _I32, _I32, _I32, _F32,
@@ -413,6 +417,44 @@ def tree_lm_head_logprobs_entropy(hidden, weight, key_reach, lse, workspace, dev
         _ptr(blockmap), 0 if blockmap is None else _nbytes(blockmap), _ptr(lse), _ptr(entropy),
         _ptr(vocab_min), _ptr(vocab_max), _ptr(logprob), _ptr(token_pred), _ptr(workspace),
         _nbytes(workspace), _ptr(dev_status), _stream_ptr(stream)))
+
+
+def lm_head_grad_workspace_bytes(rows: int) -> int:
+    return int(_lib.tree_lm_head_grad_workspace_bytes(int(rows)))
+
+
+def tree_lm_head_logits_grad(hidden, weight, key_reach, lse, grad_logits, workspace, dev_status,
+                             row_lo: int = 0, row_hi: int | None = None, token_ids=None,
+                             entropy=None, grad_logprob=None, grad_entropy=None, stream=None):
+    """Gradient of the fused gather with respect to the logits of rows
+    ``[row_lo, row_hi)`` into ``grad_logits`` (bf16 ``[rows, V]``, unit stride
+    along V), recomputing the logits tile by tile."""
+    import torch
+    _on_device(hidden=hidden, weight=weight, key_reach=key_reach, lse=lse,
+               grad_logits=grad_logits, workspace=workspace, dev_status=dev_status,
+               token_ids=token_ids, entropy=entropy, grad_logprob=grad_logprob,
+               grad_entropy=grad_entropy)
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight, torch.bfloat16, "weight")
+    T_pad, H = hidden.shape
+    V = weight.shape[0]
+    row_hi = T_pad if row_hi is None else int(row_hi)
+    if (grad_logits.dtype != torch.bfloat16 or grad_logits.dim() != 2
+            or grad_logits.stride(1) != 1 or grad_logits.shape[1] != V
+            or grad_logits.shape[0] != row_hi - int(row_lo)):
+        raise ValueError("grad_logits must be bf16 [row_hi - row_lo, V] with unit stride along V")
+    for t, n in ((key_reach, "key_reach"), (token_ids, "token_ids"), (lse, "lse"),
+                 (entropy, "entropy"), (grad_logprob, "grad_logprob"),
+                 (grad_entropy, "grad_entropy")):
+        if t is not None:
+            _need(t, torch.int32 if n in ("key_reach", "token_ids") else torch.float32, n)
+            if t.numel() != T_pad:
+                raise ValueError(f"{n} must hold T_pad = {T_pad} values")
+    _check("tree_lm_head_logits_grad", _lib.tree_lm_head_logits_grad(
+        _ptr(hidden), _ptr(weight), T_pad, H, V, int(row_lo), row_hi, _ptr(token_ids),
+        _ptr(key_reach), _ptr(lse), _ptr(entropy), _ptr(grad_logprob), _ptr(grad_entropy),
+        _ptr(grad_logits), grad_logits.stride(0), _ptr(workspace), _nbytes(workspace),
+        _ptr(dev_status), _stream_ptr(stream)))
 
 
 DTA_FWD_PUSH, DTA_FWD_BWD, DTA_BWD_POP = 0, 1, 2

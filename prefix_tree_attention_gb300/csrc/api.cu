@@ -44,6 +44,13 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_h, const CUtensorMap& tm_w, con
                            const void* blockmap, float* lse, float* entropy, float* vmin,
                            float* vmax, float* logprob, int32_t* token_pred, void* workspace,
                            int32_t* status, cudaStream_t s, int num_sms);
+cudaError_t launch_lm_head_grad(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
+                                const void* hidden, const void* weight, int32_t T_pad, int32_t H,
+                                int32_t V, int32_t row_lo, int32_t row_hi,
+                                const int32_t* token_ids, const int32_t* key_reach,
+                                const float* lse, const float* entropy, const float* g_lp,
+                                const float* g_ent, void* grad, int64_t ldg, void* workspace,
+                                int32_t* status, cudaStream_t s, int num_sms);
 
 namespace {
 std::atomic<uint64_t> g_launches{0};
@@ -433,6 +440,43 @@ tree_status_t tree_lm_head_logprobs_entropy(const void* hidden, const void* weig
                                           vocab_max, logprob, token_pred, workspace, dev_status,
                                           reinterpret_cast<cudaStream_t>(stream),
                                           num_sms_current()));
+}
+
+size_t tree_lm_head_grad_workspace_bytes(int32_t rows) {
+  return rows < 0 ? 0 : static_cast<size_t>(rows) * 16;
+}
+
+tree_status_t tree_lm_head_logits_grad(const void* hidden, const void* weight, int32_t T_pad,
+                                       int32_t H, int32_t V, int32_t row_lo, int32_t row_hi,
+                                       const int32_t* token_ids, const int32_t* key_reach,
+                                       const float* lse, const float* entropy,
+                                       const float* grad_logprob, const float* grad_entropy,
+                                       void* grad_logits, int64_t grad_row_stride,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_status, tree_stream_t stream) {
+  if (T_pad < 0 || H < 1 || V < 1 || !dev_status || grad_row_stride < V)
+    return TREE_ERR_INVALID_ARG;
+  if (row_lo < 0 || row_hi < row_lo || row_hi > T_pad) return TREE_ERR_INVALID_ARG;
+  if (T_pad % tree::kBlock || row_lo % tree::kBlock || row_hi % tree::kBlock)
+    return TREE_ERR_ALIGNMENT;
+  if (H % 64) return TREE_ERR_UNSUPPORTED;
+  if (row_hi == row_lo) return TREE_OK;
+  if (!hidden || !weight || !key_reach || !lse || !grad_logits || !workspace)
+    return TREE_ERR_INVALID_ARG;
+  if (grad_logprob && !token_ids) return TREE_ERR_INVALID_ARG;
+  if (grad_entropy && !entropy) return TREE_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(weight) || !aligned16(workspace) ||
+      !aligned16(grad_logits) || (grad_row_stride * 2) % 16)
+    return TREE_ERR_ALIGNMENT;
+  if (workspace_bytes < tree_lm_head_grad_workspace_bytes(row_hi - row_lo))
+    return TREE_ERR_WORKSPACE;
+  CUtensorMap th, tw;
+  if (!encode_map_2d(&th, hidden, T_pad, H, 128) || !encode_map_2d(&tw, weight, V, H, 256))
+    return TREE_ERR_CUDA;
+  return cuda_result(tree::launch_lm_head_grad(
+      th, tw, hidden, weight, T_pad, H, V, row_lo, row_hi, token_ids, key_reach, lse, entropy,
+      grad_logprob, grad_entropy, grad_logits, grad_row_stride, workspace, dev_status,
+      reinterpret_cast<cudaStream_t>(stream), num_sms_current()));
 }
 
 }  // extern "C"

@@ -11,7 +11,7 @@
 // memory.
 //
 // Kernels (each skips its work once *dev_status is non-zero):
-//  1 k_lmh_gemm_stats  persistent, one CTA per SM.  A work item is a block
+//  1 k_lmh_gemm<false> persistent, one CTA per SM.  A work item is a block
 //     of 128 rows and a chunk of kChunkTiles vocabulary tiles of 256
 //     columns.  Per vocabulary tile the logits accumulate in TMEM over the
 //     hidden size, 64 at a time (tcgen05.mma M = 128, N = 256, K = 16, bf16
@@ -30,6 +30,20 @@
 //  3 k_lmh_labels      one warp per token: pred(j) by the search of the
 //     gather, then the label logit as a fp32 dot product of hidden[pred(j)]
 //     and W[token_ids[j]]; logprob = dot - lse[pred(j)].
+//
+// The gradient with respect to the logits (tree_lm_head_logits_grad), for
+// a chunk of rows [row_lo, row_hi) written to a caller's [rows, V] buffer:
+//  4 k_lmh_grad_coef   one thread per row: with G the sum of the log-prob
+//     gradients of the row's children (the tokens it predicts), E its
+//     entropy gradient, every logit's gradient is -p_v (A + E x_v),
+//     A = G + E (H - lse); the row's (-lse log2 e, -E, -A).
+//  5 k_lmh_gemm<true>  the same GEMM; its epilogue turns each logits tile
+//     into its gradient p_v (-A - E x_v), p_v = 2^(x_v log2 e - lse log2 e),
+//     and stores it as bf16 (no statistics).
+//  6 k_lmh_grad_labels one warp per row: for each child j, the one-hot term
+//     g_lp[j] at the label column, on the label logit recomputed as a fp32
+//     dot product, rewritten with one rounding (a row's children carry
+//     distinct labels in a trie).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -64,8 +78,12 @@ struct LmhSmem {
 
 struct LmhParams {
   int32_t T_pad, H, V;
+  int32_t mb0;                           // first row block of the work
   int32_t n_mblk, n_ntiles, n_chunks, n_items;
-  float4* partial;                       // [2 * n_chunks][T_pad]: (m, s, t, min)
+  float4* partial;                       // statistics: [2 * n_chunks][T_pad] (m, s, t, min)
+  const float4* coef;                    // gradient: per row of the chunk (nL, nE, nA, pad)
+  __nv_bfloat16* grad;                   // gradient: [n_mblk * 128 rows, ldg] bf16
+  int64_t ldg;
   int32_t* status;
 };
 
@@ -109,9 +127,46 @@ __device__ __forceinline__ void fold64(Acc& a, const uint32_t (&r0)[32], const u
   }
 }
 
+// Gradient of 64 accumulator columns: d = 2^(x log2 e + nL) (nA + nE x),
+// stored as bf16 at dst[0 .. min(nvalid, 64)); zeros for a pad row.
+__device__ __forceinline__ void grad64(const uint32_t (&r0)[32], const uint32_t (&r1)[32],
+                                       const float4& cf, __nv_bfloat16* dst, int32_t nvalid) {
+  if (nvalid <= 0) return;
+  uint32_t o[32];
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float u0, u1, w0, w1, d0, d1;
+    const float x0 = __uint_as_float(r0[e]), x1 = __uint_as_float(r0[e + 1]);
+    fma2(u0, u1, x0, x1, kLog2e, kLog2e, cf.x, cf.x);
+    fma2(w0, w1, x0, x1, cf.y, cf.y, cf.z, cf.z);
+    mul2(d0, d1, ex2f(u0), ex2f(u1), w0, w1);
+    o[e >> 1] = pack_bf16x2(d0, d1);
+    const float y0 = __uint_as_float(r1[e]), y1 = __uint_as_float(r1[e + 1]);
+    fma2(u0, u1, y0, y1, kLog2e, kLog2e, cf.x, cf.x);
+    fma2(w0, w1, y0, y1, cf.y, cf.y, cf.z, cf.z);
+    mul2(d0, d1, ex2f(u0), ex2f(u1), w0, w1);
+    o[16 + (e >> 1)] = pack_bf16x2(d0, d1);
+  }
+  if (cf.w != 0.f) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) o[e] = 0u;
+  }
+  if (nvalid >= 64) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  } else {
+    uint16_t* d2 = reinterpret_cast<uint16_t*>(dst);
+#pragma unroll
+    for (int e = 0; e < 64; ++e)
+      if (e < nvalid) d2[e] = static_cast<uint16_t>(o[e >> 1] >> ((e & 1) * 16));
+  }
+}
+
+template <bool kGrad>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-k_lmh_gemm_stats(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
-                 const LmhParams p) {
+k_lmh_gemm(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+           const LmhParams p) {
   if (ld_status(p.status)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* aligned = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -158,7 +213,7 @@ k_lmh_gemm_stats(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
             if (kc >= kStages && !(ok = mbar_wait(&sm.empty[s], (kc / kStages - 1) & 1, ab)))
               break;
             mbar_arrive_expect_tx(&sm.full[s], kATileBytes + kBTileBytes);
-            tma_load_2d(sm.a[s], &tm_h, &sm.full[s], ks * kBK, mb * kBM);
+            tma_load_2d(sm.a[s], &tm_h, &sm.full[s], ks * kBK, (p.mb0 + mb) * kBM);
             tma_load_2d(sm.b[s], &tm_w, &sm.full[s], ks * kBK, nt * kBN);
             ++kc;
           }
@@ -215,26 +270,36 @@ k_lmh_gemm_stats(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       int32_t mb, chunk;
       item_coords(w, p, mb, chunk);
       const int32_t t0 = chunk * kChunkTiles, t1 = min(t0 + kChunkTiles, p.n_ntiles);
+      const int32_t lrow = mb * kBM + q * 32 + lane;   // row within the work's rows
       Acc a;
       acc_init(a);
+      float4 cf = make_float4(0.f, 0.f, 0.f, 1.f);
+      __nv_bfloat16* grow = nullptr;
+      if constexpr (kGrad) {
+        cf = p.coef[lrow];
+        grow = p.grad + static_cast<size_t>(lrow) * p.ldg;
+      }
       for (int32_t nt = t0; nt < t1; ++nt, ++tc) {
         const uint32_t buf = tc & 1;
         if (!(ok = mbar_wait_warp(&sm.acc_full[buf], (tc >> 1) & 1, ab))) break;
         tc_fence_after();
         const uint32_t taddr = tbase + lane_off + buf * kBN + half * 128;
-        const int32_t nvalid = p.V - (nt * kBN + half * 128);   // columns < V from here
+        const int32_t col0 = nt * kBN + half * 128;
+        const int32_t nvalid = p.V - col0;             // columns < V from here
         uint32_t r0[32], r1[32];
         tmem_ld32x2(taddr, taddr + 32, r0, r1);
-        fold64(a, r0, r1, nvalid);
+        if constexpr (kGrad) grad64(r0, r1, cf, grow + col0, nvalid);
+        else fold64(a, r0, r1, nvalid);
         tmem_ld32x2(taddr + 64, taddr + 96, r0, r1);
         tc_fence_before();
         mbar_arrive(&sm.acc_empty[buf]); // the accumulator may be overwritten now
-        fold64(a, r0, r1, nvalid - 64);
+        if constexpr (kGrad) grad64(r0, r1, cf, grow + col0 + 64, nvalid - 64);
+        else fold64(a, r0, r1, nvalid - 64);
       }
       if (!ok) break;
-      const int32_t row = mb * kBM + q * 32 + lane;
-      p.partial[static_cast<size_t>(chunk * 2 + half) * p.T_pad + row] =
-          make_float4(a.m, a.s0 + a.s1, a.t0 + a.t1, a.mn);
+      if constexpr (!kGrad)
+        p.partial[static_cast<size_t>(chunk * 2 + half) * p.T_pad + lrow] =
+            make_float4(a.m, a.s0 + a.s1, a.t0 + a.t1, a.mn);
     }
   }
   tc_fence_before();
@@ -325,6 +390,85 @@ __global__ void __launch_bounds__(kLabelWarps * 32) k_lmh_labels(
   if (lane == 0) logprob[j] = out;
 }
 
+// The next child of a row after child j (the token after j's subtree), or
+// INT32_MAX (and a MALFORMED_TREE status) if key_reach does not advance.
+__device__ __forceinline__ int32_t lmh_next_child(int32_t j, const int32_t* __restrict__ reach,
+                                                  int32_t* status) {
+  const int32_t n = reach[j] + 1;
+  if (n <= j) {
+    set_status(status, TREE_ERR_MALFORMED_TREE);
+    return INT32_MAX;
+  }
+  return n;
+}
+
+__global__ void __launch_bounds__(kCombineThreads) k_lmh_grad_coef(
+    int32_t row_lo, int32_t rows, int32_t T_pad, const int32_t* __restrict__ reach,
+    const float* __restrict__ lse, const float* __restrict__ entropy,
+    const float* __restrict__ g_lp, const float* __restrict__ g_ent, float4* __restrict__ coef,
+    int32_t* status) {
+  if (ld_status(status)) return;
+  const int32_t t = blockIdx.x * kCombineThreads + threadIdx.x;
+  if (t >= rows) return;
+  const int32_t r = row_lo + t;
+  int32_t rr = reach[r];
+  if (rr < r) {                          // pad: gradient 0
+    coef[t] = make_float4(0.f, 0.f, 0.f, 1.f);
+    return;
+  }
+  if (rr >= T_pad) {
+    set_status(status, TREE_ERR_MALFORMED_TREE);
+    rr = T_pad - 1;
+  }
+  float G = 0.f;
+  if (g_lp)
+    for (int32_t j = r + 1; j <= rr; j = lmh_next_child(j, reach, status)) G += g_lp[j];
+  const float L = lse[r];
+  const float E = g_ent ? g_ent[r] : 0.f;
+  const float H = E != 0.f ? entropy[r] : 0.f;
+  coef[t] = make_float4(-L * kLog2e, -E, -(G + E * (H - L)), 0.f);
+}
+
+__global__ void __launch_bounds__(kLabelWarps * 32) k_lmh_grad_labels(
+    const __nv_bfloat16* __restrict__ hidden, const __nv_bfloat16* __restrict__ weight,
+    int32_t H, int32_t V, int32_t T_pad, int32_t row_lo, int32_t rows,
+    const int32_t* __restrict__ token_ids, const int32_t* __restrict__ reach,
+    const float* __restrict__ g_lp, const float4* __restrict__ coef,
+    __nv_bfloat16* __restrict__ grad, int64_t ldg, int32_t* status) {
+  if (ld_status(status)) return;
+  const int lane = threadIdx.x & 31;
+  const int32_t t = blockIdx.x * kLabelWarps + (threadIdx.x >> 5);   // warp-uniform
+  if (t >= rows) return;
+  const int32_t r = row_lo + t;
+  const float4 cf = coef[t];
+  if (cf.w != 0.f) return;
+  const int32_t rr = min(reach[r], T_pad - 1);
+  const uint4* hr = reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(r) * H);
+  for (int32_t j = r + 1; j <= rr; j = lmh_next_child(j, reach, status)) {
+    const int32_t y = token_ids[j];
+    if (y < 0 || y >= V) {
+      if (lane == 0) set_status(status, TREE_ERR_MALFORMED_TREE);
+      continue;
+    }
+    const uint4* wr = reinterpret_cast<const uint4*>(weight + static_cast<size_t>(y) * H);
+    float acc0 = 0.f, acc1 = 0.f;
+    for (int32_t i = lane; i < H / 8; i += 32) {
+      const uint4 x = hr[i], w = wr[i];
+      fma2(acc0, acc1, bf_lo(x.x), bf_hi(x.x), bf_lo(w.x), bf_hi(w.x), acc0, acc1);
+      fma2(acc0, acc1, bf_lo(x.y), bf_hi(x.y), bf_lo(w.y), bf_hi(w.y), acc0, acc1);
+      fma2(acc0, acc1, bf_lo(x.z), bf_hi(x.z), bf_lo(w.z), bf_hi(w.z), acc0, acc1);
+      fma2(acc0, acc1, bf_lo(x.w), bf_hi(x.w), bf_lo(w.w), bf_hi(w.w), acc0, acc1);
+    }
+    float x = acc0 + acc1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) {
+      const float d = fmaf(ex2f(fmaf(x, kLog2e, cf.x)), fmaf(x, cf.y, cf.z), g_lp[j]);
+      grad[static_cast<size_t>(t) * ldg + y] = __float2bfloat16_rn(d);
+    }
+  }
+}
+
 }  // namespace
 
 size_t lm_head_workspace_bytes(int32_t T_pad, int32_t V) {
@@ -347,15 +491,19 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_h, const CUtensorMap& tm_w, con
   p.n_ntiles = (V + kBN - 1) / kBN;
   p.n_chunks = (p.n_ntiles + kChunkTiles - 1) / kChunkTiles;
   p.n_items = p.n_mblk * p.n_chunks;
+  p.mb0 = 0;
   p.partial = static_cast<float4*>(workspace);
+  p.coef = nullptr;
+  p.grad = nullptr;
+  p.ldg = 0;
   p.status = status;
   const size_t smem = sizeof(LmhSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_lmh_gemm_stats,
+  cudaError_t e = cudaFuncSetAttribute(k_lmh_gemm<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < num_sms ? p.n_items : num_sms;
-  k_lmh_gemm_stats<<<grid, kGemmThreads, smem, s>>>(tm_h, tm_w, p);
+  k_lmh_gemm<false><<<grid, kGemmThreads, smem, s>>>(tm_h, tm_w, p);
   k_lmh_combine<<<(T_pad + kCombineThreads - 1) / kCombineThreads, kCombineThreads, 0, s>>>(
       p.partial, 2 * p.n_chunks, T_pad, key_reach, lse, entropy, vmin, vmax, status);
   int launches = 2;
@@ -364,6 +512,49 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_h, const CUtensorMap& tm_w, con
     k_lmh_labels<<<T_pad / kLabelWarps, kLabelWarps * 32, 0, s>>>(
         static_cast<const __nv_bfloat16*>(hidden), static_cast<const __nv_bfloat16*>(weight), H,
         V, token_ids, key_reach, bm, lse, logprob, token_pred, status);
+    ++launches;
+  }
+  count_launches(launches);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lm_head_grad(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
+                                const void* hidden, const void* weight, int32_t T_pad, int32_t H,
+                                int32_t V, int32_t row_lo, int32_t row_hi,
+                                const int32_t* token_ids, const int32_t* key_reach,
+                                const float* lse, const float* entropy, const float* g_lp,
+                                const float* g_ent, void* grad, int64_t ldg, void* workspace,
+                                int32_t* status, cudaStream_t s, int num_sms) {
+  const int32_t rows = row_hi - row_lo;
+  LmhParams p;
+  p.T_pad = T_pad;
+  p.H = H;
+  p.V = V;
+  p.mb0 = row_lo / kBM;
+  p.n_mblk = rows / kBM;
+  p.n_ntiles = (V + kBN - 1) / kBN;
+  p.n_chunks = (p.n_ntiles + kChunkTiles - 1) / kChunkTiles;
+  p.n_items = p.n_mblk * p.n_chunks;
+  p.partial = nullptr;
+  p.coef = static_cast<const float4*>(workspace);
+  p.grad = static_cast<__nv_bfloat16*>(grad);
+  p.ldg = ldg;
+  p.status = status;
+  k_lmh_grad_coef<<<(rows + kCombineThreads - 1) / kCombineThreads, kCombineThreads, 0, s>>>(
+      row_lo, rows, T_pad, key_reach, lse, entropy, g_lp, g_ent,
+      static_cast<float4*>(workspace), status);
+  const size_t smem = sizeof(LmhSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_lmh_gemm<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = p.n_items < num_sms ? p.n_items : num_sms;
+  k_lmh_gemm<true><<<grid, kGemmThreads, smem, s>>>(tm_h, tm_w, p);
+  int launches = 2;
+  if (g_lp) {
+    k_lmh_grad_labels<<<(rows + kLabelWarps - 1) / kLabelWarps, kLabelWarps * 32, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(hidden), static_cast<const __nv_bfloat16*>(weight), H,
+        V, T_pad, row_lo, rows, token_ids, key_reach, g_lp, p.coef, p.grad, ldg, status);
     ++launches;
   }
   count_launches(launches);

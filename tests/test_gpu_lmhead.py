@@ -213,3 +213,176 @@ def test_fused_qwen3_head_sampled(name):
     hidden, weight = W.lm_head(packed.T_pad, QWEN3_HIDDEN, QWEN3_VOCAB, seed=3, device=DEV)
     run = _Run(packed, hidden, weight)
     _check(packed, hidden, weight, run, rows=_sample(packed, 24, 9))
+
+
+# ------------------------------------------------------------------ gradient
+HALF_ULP_BF16 = 2.0 ** -8   # unit roundoff of bf16
+
+
+def _seq_grads(packed, seed, lp=True, ent=True):
+    rng = np.random.default_rng(seed)
+    return {s: (rng.standard_normal(len(packed.seq_index[s]) - 1) if lp else None,
+                rng.standard_normal(len(packed.seq_index[s]) - 1) if ent else None)
+            for s in packed.seq_ids}
+
+
+def _packed_grads(packed, grads):
+    T = packed.T_pad
+    tok, row, tok_abs = np.zeros(T), np.zeros(T), np.zeros(T)
+    for s, (a, b) in grads.items():
+        idx = np.asarray(packed.seq_index[s])
+        if a is not None:
+            np.add.at(tok, idx[1:], a)
+            np.add.at(tok_abs, idx[1:], np.abs(a))
+        if b is not None:
+            np.add.at(row, idx[:-1], b)
+    return tok, row, tok_abs
+
+
+class _HostLogits:
+    """Rows of the LM-head logits, float64, computed on demand."""
+
+    def __init__(self, h, w):
+        self.h, self.w = h, w
+
+    def __getitem__(self, r):
+        return OL.lm_head_logits(self.h[int(r):int(r) + 1].astype(np.float64), self.w)[0]
+
+
+def _run_grad(packed, hidden, weight, grads, chunks, with_lp=True, with_ent=True):
+    """Fused forward, the merge adjoints on the device, then the chunked
+    logits gradient; returns {row: gradient row (float64)} and the run."""
+    run = _Run(packed, hidden, weight)
+    assert int(run.bufs.status.item()) == 0
+    T, V = packed.T_pad, weight.shape[0]
+    n_seqs = max(packed.seq_ids) + 1
+    pos, offs = ptg.sequence_index_arrays([packed], n_seqs, [0])
+    max_len = max(len(packed.seq_index[s]) for s in packed.seq_ids) - 1
+    g_lp = np.full((n_seqs, max_len), np.nan, np.float32)
+    g_ent = np.full((n_seqs, max_len), np.nan, np.float32)
+    for s, (a, b) in grads.items():
+        n = len(packed.seq_index[s]) - 1
+        g_lp[s, :n] = 0.0 if a is None else a
+        g_ent[s, :n] = 0.0 if b is None else b
+    f = dict(dtype=torch.float32, device=DEV)
+    tok_g, row_g = torch.zeros(T, **f), torch.zeros(T, **f)
+    st = run.bufs.status
+    pos_d, offs_d = _dev(pos), _dev(offs, torch.int64)
+    ptg.tree_merge_per_sequence_bwd(_dev(g_lp, torch.float32), pos_d, offs_d, tok_g, st, 1, 1)
+    ptg.tree_merge_per_sequence_bwd(_dev(g_ent, torch.float32), pos_d, offs_d, row_g, st, 0, 1)
+    out = {}
+    width = (V + 7) // 8 * 8                  # rows 16-byte aligned, as the call requires
+    for lo, hi in chunks:
+        gbuf = torch.full((hi - lo, width), float("nan"), dtype=torch.bfloat16, device=DEV)
+        grad = gbuf[:, :V]
+        ws = torch.empty(ptg.lm_head_grad_workspace_bytes(hi - lo) // 4, **f)
+        ptg.tree_lm_head_logits_grad(
+            hidden, weight, run.bufs.key_reach, run.lse, grad, ws, st, lo, hi,
+            token_ids=_dev(run.tok), entropy=run.ent,
+            grad_logprob=tok_g if with_lp else None, grad_entropy=row_g if with_ent else None)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, ptg.status_string(int(st.item()))
+        assert torch.isnan(gbuf[:, V:].float()).all()       # past V: untouched
+        g = grad.float().cpu().numpy().astype(np.float64)
+        for r in range(lo, hi):
+            out[r] = g[r - lo]
+    return out, run
+
+
+def _check_grad(packed, hidden, weight, grads, got, rows):
+    """Kernel gradient rows against the oracle within the derived bound:
+    p (|w| (2 delta + LSE_TOL + 1e-5) + 1e-6 Gabs + |E| (ENT_TOL + LSE_TOL + 4 delta)
+       + 1e-6 (|A| + |E x|)) + a bf16 unit roundoff of |d|, delta as for the forward."""
+    h = hidden.float().cpu().numpy()
+    w = weight.float().cpu().numpy().astype(np.float64)
+    H = h.shape[1]
+    w_norm = np.sqrt((w * w).sum(axis=1)).max()
+    tok, row, tok_abs = _packed_grads(packed, grads)
+    pred = OL.token_pred(packed)
+    tok_ids = np.where(packed.token_ids >= 0, packed.token_ids % w.shape[0], -1)
+    pk = _Relabel(packed, tok_ids)
+    want_rows = OL.gather_packed_tree_backward(_HostLogits(h, w), pk, grads, rows=rows)
+    for r in rows:
+        g = got[r]
+        if packed.token_node[r] < 0:
+            assert (g == 0).all(), r
+            continue
+        x = _HostLogits(h, w)[r]
+        lq = OL.log_softmax(x)
+        p = np.exp(lq)
+        lse = float(x.max() + np.log(np.exp(x - x.max()).sum()))
+        Hr = float(-(p * lq).sum())
+        kids = np.nonzero(pred == r)[0]
+        G, Gabs, E = float(tok[kids].sum()), float(tok_abs[kids].sum()), float(row[r])
+        A = G + E * (Hr - lse)
+        wv = -(A + E * x)
+        d = 2.0 ** -24 * (H / 16) * np.sqrt((h[r].astype(np.float64) ** 2).sum()) * w_norm
+        tol = p * (np.abs(wv) * (2 * d + LSE_TOL + 1e-5) + 1e-6 * Gabs
+                   + abs(E) * (ENT_TOL + LSE_TOL + 4 * d) + 1e-6 * (abs(A) + np.abs(E * x)))
+        want = want_rows[r]
+        tol += 1.01 * HALF_ULP_BF16 * np.abs(want) + 1e-30
+        for j in kids:
+            tol[int(tok_ids[j])] += 1e-7 * abs(tok[j]) + 1e-6 * tok_abs[j]
+        bad = np.abs(g - want) > tol
+        assert not bad.any(), (r, np.nonzero(bad)[0][:5], g[bad][:5], want[bad][:5])
+
+
+class _Relabel:
+    """The packed trie with its token ids folded into the vocabulary."""
+
+    def __init__(self, packed, tok):
+        self.__dict__.update(packed.__dict__)
+        self.token_ids = tok
+
+
+@pytest.mark.parametrize("H,V,with_lp,with_ent", [
+    (128, 1000, True, True),
+    (256, 2055, True, True),
+    (64, 300, True, False),
+    (64, 300, False, True),
+])
+def test_logits_grad_matches_oracle(H, V, with_lp, with_ent):
+    rng = W.SplitMix64(H * 7 + V)
+    seqs = W.random_sequences(rng, 10, 90, 3)
+    (packed,) = OT.pack_sequences(seqs, 4096)
+    hidden, weight = W.lm_head(packed.T_pad, H, V, seed=V, device=DEV)
+    grads = _seq_grads(packed, seed=H, lp=with_lp, ent=with_ent)
+    got, _ = _run_grad(packed, hidden, weight, grads, [(0, packed.T_pad)], with_lp, with_ent)
+    _check_grad(packed, hidden, weight, grads, got, list(range(packed.T_pad)))
+
+
+def test_logits_grad_in_chunks_and_fanout():
+    # chunks that start past row 0 and end before T_pad; a 40-child fan-out
+    # whose branch row sits in the first chunk while its children do not
+    rng = W.SplitMix64(19)
+    prefix = [rng.randint(1, 30) for _ in range(100)]
+    seqs = [prefix + [100 + k] + [rng.randint(1, 900) for _ in range(rng.randint(0, 30))]
+            for k in range(40)]
+    seqs += W.random_sequences(rng, 8, 120, 2)
+    (packed,) = OT.pack_sequences(seqs, 4096)
+    T = packed.T_pad
+    assert T >= 384
+    hidden, weight = W.lm_head(T, 192, 1500, seed=4, device=DEV)
+    grads = _seq_grads(packed, seed=5)
+    chunks = [(0, 128), (128, 384), (384, T)] if T > 384 else [(0, 128), (128, 384)]
+    got, _ = _run_grad(packed, hidden, weight, grads, chunks)
+    _check_grad(packed, hidden, weight, grads, got, list(range(T)))
+
+
+def test_logits_grad_qwen3_head_sampled():
+    """Qwen3-8B's head (H = 4096, V = 151,936) on the tiny workload: the
+    gradient of rows [0, 512) and [1024, T_pad), sampled rows against the
+    oracle (the widest branch rows, random rows, a pad)."""
+    wl = W.WORKLOADS["tiny"]
+    (packed,) = OT.pack_sequences(W.sequences("tiny"), wl.max_tokens_per_mb)
+    T = packed.T_pad
+    hidden, weight = W.lm_head(T, QWEN3_HIDDEN, QWEN3_VOCAB, seed=6, device=DEV)
+    grads = _seq_grads(packed, seed=7)
+    got, _ = _run_grad(packed, hidden, weight, grads, [(0, 512), (1024, T)])
+    pred = OL.token_pred(packed)
+    kids = np.bincount(pred[pred >= 0], minlength=T)
+    rng = W.SplitMix64(8)
+    rows = {int(r) for r in np.argsort(-kids)[:3]} | {rng.randint(0, 511) for _ in range(6)}
+    rows |= {rng.randint(1024, packed.n_tokens - 1) for _ in range(4)} | {T - 1}
+    rows = sorted(r for r in rows if r < 512 or r >= 1024)
+    _check_grad(packed, hidden, weight, grads, got, rows)

@@ -1035,6 +1035,94 @@ def lmhead_oracle_rate(budget_s: float, seed: int, rows: int = 16, H: int = QWEN
     return rec["rate"], rec["sample"]
 
 
+def lmhead_backward(ptg, cases, offs, hidden, weight, lse_all, ent_all, pos_d, soffs_d,
+                    merged_shape, tokens, flops, seed, args, ws, peaks):
+    """The fused gather's gradient with respect to the logits over the same
+    batch: per-sequence gradients of log-probabilities and entropies
+    ([n_seqs, max_len], fp32 N(0, 1)) through the two merge adjoints, then
+    tree_lm_head_logits_grad over every trie's rows as one chunk into one bf16
+    [T_pad, V] buffer (the logits tiles recomputed in TMEM).  The LM head's own
+    gradients (two plain GEMMs of that buffer) are the model's and not timed."""
+    import torch
+    device = hidden.device
+    g = torch.Generator(device=device)
+    g.manual_seed(2000 + seed)
+    g_lp = torch.randn(merged_shape, generator=g, device=device, dtype=torch.float32)
+    g_ent = torch.randn(merged_shape, generator=g, device=device, dtype=torch.float32)
+    tok_g = torch.empty(offs[-1], dtype=torch.float32, device=device)
+    row_g = torch.empty_like(tok_g)
+    t_max = hidden.shape[0]
+    V = weight.shape[0]
+    grad = torch.empty((t_max, (V + 7) // 8 * 8), dtype=torch.bfloat16, device=device)[:, :V]
+    gws = torch.empty(ptg.lm_head_grad_workspace_bytes(t_max) // 4, dtype=torch.float32,
+                      device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def rows(i, tr, bufs, tok):
+        sl = slice(offs[i], offs[i + 1])
+        ptg.tree_lm_head_logits_grad(hidden[:tr.T_pad], weight, bufs.key_reach, lse_all[sl],
+                                     grad[:tr.T_pad], gws, bufs.status, 0, tr.T_pad,
+                                     token_ids=tok, entropy=ent_all[sl], grad_logprob=tok_g[sl],
+                                     grad_entropy=row_g[sl])
+
+    def step():
+        tok_g.zero_()
+        row_g.zero_()
+        ptg.tree_merge_per_sequence_bwd(g_lp, pos_d, soffs_d, tok_g, status, 1, 1)
+        ptg.tree_merge_per_sequence_bwd(g_ent, pos_d, soffs_d, row_g, status, 0, 1)
+        for i, (tr, bufs, tok) in enumerate(cases):
+            rows(i, tr, bufs, tok)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    bad = [int(b.status.item()) for _, b, _ in cases] + [int(status.item())]
+    if any(bad):
+        raise RuntimeError("device status " + ptg.status_string(max(bad)))
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    launches0 = ptg.launch_count()
+    barrier(ws)
+    torch.cuda.synchronize()
+    per_step = []
+    for _ in range(args.steps):
+        s0, s1 = mk(), mk()
+        s0.record(stream)
+        step()
+        s1.record(stream)
+        per_step.append((s0, s1))
+    torch.cuda.synchronize()
+    barrier(ws)
+    launches = ptg.launch_count() - launches0
+    ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in per_step])), ws)
+    call_ms = 0.0
+    for i, (tr, bufs, tok) in enumerate(cases):
+        e0, e1 = mk(), mk()
+        e0.record(stream)
+        rows(i, tr, bufs, tok)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        call_ms += e0.elapsed_time(e1)
+    achieved = flops / (call_ms * 1e-3) / 1e12
+    return {
+        "what": "merge adjoints + logits gradient of every trie (logits recomputed in TMEM)",
+        "ms_per_step": round(ms, 3),
+        "tokens_per_s": round(sum_over_ranks(tokens, ws) / (ms * 1e-3), 1),
+        "gpu_launches": launches,
+        "grad_gb_written_per_step": round(sum(tr.T_pad for tr, _, _ in cases) * V * 2 / 1e9, 2),
+        "roofline": {
+            "kernel": "k_lmh_gemm<true> (LM-head GEMM + logits-gradient epilogue) with its "
+                      "coefficient and one-hot passes",
+            "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16"],
+            "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
+            "peak_kind": f"bf16 dense, burst ({peaks['source']})",
+            "frac_of_sustained": round(achieved / peaks["bf16_sustained"], 4),
+            "traffic": None, "avg_launch_ms": round(call_ms / len(cases), 4),
+            "flops_per_launch": flops / len(cases),
+        },
+    }
+
+
 def run_lmhead(args, rank, ws):
     """``--path lmhead``: the LM head fused with the log-prob gather.
 
@@ -1141,6 +1229,9 @@ def run_lmhead(args, rank, ws):
     peaks = measured_peaks()
     achieved = flops / (gemm_ms * 1e-3) / 1e12
     step_tflops = sum_over_ranks(flops, ws) / (ms_max * 1e-3) / 1e12
+    backward = None if args.no_extra else lmhead_backward(
+        ptg, cases, offs, hidden, weight, lse_all, ent_all, pos_d, soffs_d,
+        (len(used), max_len), tokens, flops, seed, args, ws, peaks)
     line = {
         "metric": LMHEAD_METRIC, "value": round(tokens_all / (ms_max * 1e-3), 1),
         "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -1158,7 +1249,7 @@ def run_lmhead(args, rank, ws):
                             else f"replicas x{ws}"),
         },
         "roofline": {
-            "kernel": "k_lmh_gemm_stats (LM-head GEMM + row statistics) with k_lmh_combine",
+            "kernel": "k_lmh_gemm<false> (LM-head GEMM + row statistics) with k_lmh_combine",
             "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16"],
             "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
             "peak_kind": f"bf16 dense, burst ({peaks['source']})",
@@ -1169,6 +1260,7 @@ def run_lmhead(args, rank, ws):
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "e2e": None,
+        "backward": backward,
     }
     if rank == 0 and not args.no_cpu_baseline:
         rate, desc = lmhead_oracle_rate(min(args.cpu_budget, 15.0), seed)
@@ -1345,7 +1437,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the timed agent / long / fanout entries of config.per_workload "
-                         "and the backward object of the log-prob line")
+                         "and the backward objects of the log-prob and lmhead lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")

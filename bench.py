@@ -1297,44 +1297,54 @@ def run_e2e(ptg, cases, ws_bwds, streams, args, ws, flops_all):
         flops_all = sum_over_ranks(
             (FWD_FLOPS_PER_PAIR + BWD_FLOPS_PER_PAIR) * cases[0].d * cases[0].Hq *
             sum(c.pairs for c in cases), ws)
-    host_in = [[t.cpu().pin_memory() for t in c.input_tensors()] for c in cases]
-    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in c.output_tensors()]
-                for c in cases]
+    slab_in = _PinnedSlab(sum(_padded(t) for c in cases for t in c.input_tensors()))
+    slab_out = _PinnedSlab(sum(_padded(t) for c in cases for t in c.output_tensors()))
+    host_in = [[slab_in.take(t) for t in c.input_tensors()] for c in cases]
+    for c, hs in zip(cases, host_in):
+        for dst, src in zip(hs, c.input_tensors()):
+            dst.copy_(src)
+    host_out = [[slab_out.take(t) for t in c.output_tensors()] for c in cases]
     h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
     d2h = sum(t.numel() * t.element_size() for hs in host_out for t in hs)
     copy_in = torch.cuda.Stream()
     copy_out = torch.cuda.Stream()
 
     n_streams = len(streams)
+    # Per-trie events of the previous step: trie i's uploads may start once
+    # its previous compute has consumed the inputs, and its compute once its
+    # previous outputs are downloaded, so consecutive steps pipeline on the
+    # host link instead of draining at every step boundary.
+    prev_compute = [None] * len(cases)
+    prev_download = [None] * len(cases)
 
     def e2e_step():
-        # outputs of the previous step must be downloaded before they are rewritten
-        for st in streams:
-            st.wait_stream(copy_out)
         ready = []
         for i, c in enumerate(cases):
+            if prev_compute[i] is not None:
+                copy_in.wait_event(prev_compute[i])
             with torch.cuda.stream(copy_in):
                 for dst, src in zip(c.input_tensors(), host_in[i]):
                     dst.copy_(src, non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(copy_in)
             ready.append(ev)
-        done = []
         for i, c in enumerate(cases):
             st = streams[i % n_streams]
             st.wait_event(ready[i])
+            if prev_download[i] is not None:
+                st.wait_event(prev_download[i])
             with torch.cuda.stream(st):
                 run_path(ptg, c, ws_bwds[i % n_streams], st)
                 ev = torch.cuda.Event()
                 ev.record(st)
-            done.append(ev)
+            prev_compute[i] = ev
             copy_out.wait_event(ev)
             with torch.cuda.stream(copy_out):
                 for dst, src in zip(host_out[i], c.output_tensors()):
                     dst.copy_(src, non_blocking=True)
-        # the next step's uploads must not overwrite inputs still in use
-        for st in streams:
-            copy_in.wait_stream(st)
+                dev = torch.cuda.Event()
+                dev.record(copy_out)
+            prev_download[i] = dev
 
     for _ in range(max(1, min(args.warmup, 2))):
         e2e_step()
@@ -1393,11 +1403,64 @@ def run_e2e(ptg, cases, ws_bwds, streams, args, ws, flops_all):
            "copy_frac": round(both_s / dt, 4),
            "timing": "host wall clock around the steps, synchronised at both ends",
            "copies": "pinned host -> device inputs (token_node, entry, exit, q, k, v, do); "
-                     "device -> pinned host outputs (o, dq, dk, dv); copy streams overlap compute",
+                     "device -> pinned host outputs (o, dq, dk, dv); copy streams overlap compute, "
+                     "consecutive steps chained per trie",
            "route": "the Python binding's ctypes calls of the C ABI, torch doing the copies"}
+    rec["host_buffers"] = ("one exact-size page-locked slab per direction "
+                           f"({slab_in.kind}; {round(slab_in.nbytes / 1e9, 2)} GB in, "
+                           f"{round(slab_out.nbytes / 1e9, 2)} GB out)")
     if subset:
         rec["tries"] = f"first {len(cases)} tries (pinned buffers limited to 40% of host memory)"
+    del host_in, host_out
+    slab_in.close()
+    slab_out.close()
     return rec
+
+
+def _padded(t) -> int:
+    return (t.numel() * t.element_size() + 255) // 256 * 256
+
+
+class _PinnedSlab:
+    """One exact-size page-locked host buffer, handed out as tensors.
+
+    An anonymous mapping registered with cudaHostRegister: the pinned
+    footprint is the bytes the step moves (torch's pinned-memory allocator
+    rounds every allocation up to a power of two, which nearly doubles the
+    footprint of this leg, and a large pinned footprint slows the host link
+    on these machines).  Falls back to one torch pinned tensor if
+    registration is refused."""
+
+    def __init__(self, nbytes: int):
+        import mmap
+        import torch
+        self.nbytes = max(int(nbytes), 256)
+        self.off = 0
+        self._mm = mmap.mmap(-1, self.nbytes)
+        self._np = np.frombuffer(self._mm, dtype=np.uint8)
+        self.base = torch.from_numpy(self._np)
+        self._ptr = self.base.data_ptr()
+        rt = torch.cuda.cudart()
+        self.registered = rt.cudaHostRegister(self._ptr, self.nbytes, 0) == rt.cudaError.success
+        self.kind = "anonymous mapping + cudaHostRegister"
+        if not self.registered:
+            self.base = torch.empty(self.nbytes, dtype=torch.uint8, pin_memory=True)
+            self.kind = "torch pinned tensor"
+
+    def take(self, like):
+        import torch
+        n = like.numel() * like.element_size()
+        view = self.base[self.off:self.off + n]
+        self.off += _padded(like)
+        return view.view(like.dtype).view(like.shape) if n else torch.empty(
+            like.shape, dtype=like.dtype)
+
+    def close(self):
+        import torch
+        if self.registered:
+            torch.cuda.synchronize()
+            torch.cuda.cudart().cudaHostUnregister(self._ptr)
+            self.registered = False
 
 
 def _mem_available_bytes():

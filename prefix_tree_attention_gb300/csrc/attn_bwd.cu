@@ -392,9 +392,17 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < 64; ++c)
           if (!(lo <= q0 + c && q0 + c <= hi)) pv[c] = 0.f;
       }
+      {
+        // P^T (bf16) over the S^T columns just read, while dP^T is still
+        // being computed: off the path that waits for dP^T.
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+        tmem_st32(tbase + lane_off + kS + w * 64, pk);
+      }
       if (!(ok = mbar_wait_warp(&sm.dp_full, n & 1, ab))) break;
       tc_fence_after();
-      uint32_t pk[32], dsw[32];
+      uint32_t dsw[32];
       {
         const float4* dd4 = reinterpret_cast<const float4*>(sm.dd[s] + w * 64);
         uint32_t ra[32], rb[32];
@@ -413,14 +421,11 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                  d4.z, d4.w);
             mul2(ds0, ds1, pv[c + 0], pv[c + 1], t0, t1);
             mul2(ds2, ds3, pv[c + 2], pv[c + 3], t2, t3);
-            pk[c2 * 16 + 2 * e4] = pack_bf16x2(pv[c], pv[c + 1]);
-            pk[c2 * 16 + 2 * e4 + 1] = pack_bf16x2(pv[c + 2], pv[c + 3]);
             dsw[c2 * 16 + 2 * e4] = pack_bf16x2(ds0, ds1);
             dsw[c2 * 16 + 2 * e4 + 1] = pack_bf16x2(ds2, ds3);
           }
         }
       }
-      tmem_st32(tbase + lane_off + kS + w * 64, pk);
       tmem_st32(tbase + lane_off + kS + w * 64 + 32, dsw);
       // dS^T row r, queries w*64 .. w*64+63 -> swizzled [key][query] half w.
       // The tile staged the previous pair's dQ: the dQ warps release it once

@@ -120,8 +120,11 @@ __device__ __forceinline__ float half_max(uint32_t s_addr, int c2, int32_t j0, i
 // Scores c2*64 .. c2*64+63 of a tile against the reference max m (log2
 // units): P = 2^(s*scale*log2e - m) as 32 bf16 pairs in pk, their fp32 sum
 // added to ls.  Paired fp32 math and two independent sum chains.  Returns,
-// warp-uniformly, whether any row of the warp has a score more than the
-// threshold above m, tested on the packed bf16 P itself (P > 2^threshold).
+// warp-uniformly, whether some row of the warp may have a score more than
+// the threshold above m: the half's sum of P exceeds 2^threshold (or is not
+// a number).  Every P is >= 0, so a P above 2^threshold always trips it; a
+// sum that exceeds it without such a P only sends the tile down the exact
+// path, which recomputes the same values when the max has not grown.
 template <bool kMasked>
 __device__ __forceinline__ bool score_half(uint32_t s_addr, int c2, int32_t j0, int32_t i,
                                            const int32_t* rch, float sl2, float m,
@@ -131,7 +134,6 @@ __device__ __forceinline__ bool score_half(uint32_t s_addr, int c2, int32_t j0, 
   uint32_t ra[32], rb[32];
   tmem_ld32x2(s_addr + c2 * 64, s_addr + c2 * 64 + 32, ra, rb);
   float lt[4] = {0.f, 0.f, 0.f, 0.f};
-  uint32_t pmax[2] = {0u, 0u};
   const float nm = -m;
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
@@ -148,12 +150,10 @@ __device__ __forceinline__ bool score_half(uint32_t s_addr, int c2, int32_t j0, 
     const int a = e & 1;
     add2(lt[2 * a], lt[2 * a + 1], lt[2 * a], lt[2 * a + 1], p0, p1);
     pk[e] = pack_bf16x2(p0, p1);
-    pmax[a] = max_bf16x2(pmax[a], pk[e]);
   }
-  ls += (lt[0] + lt[1]) + (lt[2] + lt[3]);
-  const uint32_t pm = max_bf16x2(pmax[0], pmax[1]);
-  const float pmx = fmaxf(__uint_as_float(pm << 16), __uint_as_float(pm & 0xffff0000u));
-  return __any_sync(0xffffffffu, pmx > kGrowthLimit);
+  const float hs = (lt[0] + lt[1]) + (lt[2] + lt[3]);
+  ls += hs;
+  return __any_sync(0xffffffffu, !(hs <= kGrowthLimit));
 }
 
 // O *= alpha (per row) in TMEM; warp-collective.

@@ -45,7 +45,8 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_h, const CUtensorMap& tm_w, con
                            float* vmax, float* logprob, int32_t* token_pred, void* workspace,
                            int32_t* status, cudaStream_t s, int num_sms);
 cudaError_t launch_lm_head_grad(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
-                                const void* hidden, const void* weight, int32_t T_pad, int32_t H,
+                                const CUtensorMap& tm_g, const void* hidden, const void* weight,
+                                int32_t T_pad, int32_t H,
                                 int32_t V, int32_t row_lo, int32_t row_hi,
                                 const int32_t* token_ids, const int32_t* key_reach,
                                 const float* lse, const float* entropy, const float* g_lp,
@@ -131,6 +132,22 @@ bool encode_map_2d(CUtensorMap* map, const void* base, int64_t rows, int32_t col
   if (!fn) return false;
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                   strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The bf16 logits gradient [rows, V] (row stride ld elements) as a 2-D
+// TMA map for stores of 32 x 32 boxes, 64-byte swizzle; columns past V and
+// rows past the chunk are not written.
+bool encode_map_grad(CUtensorMap* map, void* base, int32_t rows, int32_t V, int64_t ld) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t elem[2] = {1, 1};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, elem,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -470,11 +487,12 @@ tree_status_t tree_lm_head_logits_grad(const void* hidden, const void* weight, i
     return TREE_ERR_ALIGNMENT;
   if (workspace_bytes < tree_lm_head_grad_workspace_bytes(row_hi - row_lo))
     return TREE_ERR_WORKSPACE;
-  CUtensorMap th, tw;
-  if (!encode_map_2d(&th, hidden, T_pad, H, 128) || !encode_map_2d(&tw, weight, V, H, 256))
+  CUtensorMap th, tw, tg;
+  if (!encode_map_2d(&th, hidden, T_pad, H, 128) || !encode_map_2d(&tw, weight, V, H, 256) ||
+      !encode_map_grad(&tg, grad_logits, row_hi - row_lo, V, grad_row_stride))
     return TREE_ERR_CUDA;
   return cuda_result(tree::launch_lm_head_grad(
-      th, tw, hidden, weight, T_pad, H, V, row_lo, row_hi, token_ids, key_reach, lse, entropy,
+      th, tw, tg, hidden, weight, T_pad, H, V, row_lo, row_hi, token_ids, key_reach, lse, entropy,
       grad_logprob, grad_entropy, grad_logits, grad_row_stride, workspace, dev_status,
       reinterpret_cast<cudaStream_t>(stream), num_sms_current()));
 }

@@ -39,7 +39,8 @@
 //     A = G + E (H - lse); the row's (-lse log2 e, -E, -A).
 //  5 k_lmh_gemm<true>  the same GEMM; its epilogue turns each logits tile
 //     into its gradient p_v (-A - E x_v), p_v = 2^(x_v log2 e - lse log2 e),
-//     and stores it as bf16 (no statistics).
+//     as bf16, each warp's 32 x 32 blocks staged in shared memory and
+//     written by bulk tensor stores (no statistics).
 //  6 k_lmh_grad_labels one warp per row: for each child j, the one-hot term
 //     g_lp[j] at the label column, on the label logit recomputed as a fp32
 //     dot product, rewritten with one rounding (a row's children carry
@@ -66,9 +67,12 @@ constexpr uint32_t kBTileBytes = kBN * kBK * 2;
 constexpr int kCombineThreads = 256;
 constexpr int kLabelWarps = 8;
 
+constexpr int kOutBox = 32;              // gradient store box: 32 rows x 32 columns (bf16)
+
 struct LmhSmem {
   uint8_t a[kStages][kATileBytes];       // 1024-byte aligned (the struct is)
   uint8_t b[kStages][kBTileBytes];
+  uint8_t out[kEpiThreads / 32][kOutBox * kOutBox * 2];   // per epilogue warp, 64-byte swizzled
   uint64_t full[kStages], empty[kStages];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t drain;
@@ -127,12 +131,10 @@ __device__ __forceinline__ void fold64(Acc& a, const uint32_t (&r0)[32], const u
   }
 }
 
-// Gradient of 64 accumulator columns: d = 2^(x log2 e + nL) (nA + nE x),
-// stored as bf16 at dst[0 .. min(nvalid, 64)); zeros for a pad row.
+// Gradient of 64 accumulator columns, d = 2^(x log2 e + nL) (nA + nE x),
+// packed as 32 bf16 pairs; zeros for a pad row.
 __device__ __forceinline__ void grad64(const uint32_t (&r0)[32], const uint32_t (&r1)[32],
-                                       const float4& cf, __nv_bfloat16* dst, int32_t nvalid) {
-  if (nvalid <= 0) return;
-  uint32_t o[32];
+                                       const float4& cf, uint32_t (&o)[32]) {
 #pragma unroll
   for (int e = 0; e < 32; e += 2) {
     float u0, u1, w0, w1, d0, d1;
@@ -151,22 +153,49 @@ __device__ __forceinline__ void grad64(const uint32_t (&r0)[32], const uint32_t 
 #pragma unroll
     for (int e = 0; e < 32; ++e) o[e] = 0u;
   }
-  if (nvalid >= 64) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
+}
+
+// One 32 x 32 block of the gradient (this warp's 32 rows, 32 columns from
+// col) through the warp's staging buffer: each lane writes its row's 64
+// bytes in the 64-byte-swizzled layout of the store's tensor map (16-byte
+// chunk c of row r at chunk c ^ ((r >> 1) & 3)), then one lane issues the
+// bulk tensor store.  The buffer is reused once the previous store has read
+// it.  Blocks that start at or past V are skipped.  The block that holds
+// column V - 1 with columns past it is written element by element instead:
+// the bulk store bounds the row in whole 16-byte units, which would write
+// into a row stride's padding past V.
+__device__ __forceinline__ void store_block(const CUtensorMap* tm_g, uint8_t* buf,
+                                            const uint32_t* w16, int32_t col, int32_t row0,
+                                            int32_t V, int lane, __nv_bfloat16* grad,
+                                            int64_t ldg) {
+  if (col >= V) return;                  // warp-uniform
+  if (col + 32 > V) {                    // warp-uniform: the last, partial block
+    uint16_t* d2 = reinterpret_cast<uint16_t*>(grad + static_cast<size_t>(row0 + lane) * ldg +
+                                               col);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) d4[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-  } else {
-    uint16_t* d2 = reinterpret_cast<uint16_t*>(dst);
+    for (int e = 0; e < 32; ++e)
+      if (col + e < V) d2[e] = static_cast<uint16_t>(w16[e >> 1] >> ((e & 1) * 16));
+    return;
+  }
+  if (lane == 0) bulk_wait_read();
+  __syncwarp();
+  uint8_t* row = buf + lane * 64;
 #pragma unroll
-    for (int e = 0; e < 64; ++e)
-      if (e < nvalid) d2[e] = static_cast<uint16_t>(o[e >> 1] >> ((e & 1) * 16));
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(row + ((c ^ ((lane >> 1) & 3)) << 4)) =
+        make_uint4(w16[4 * c], w16[4 * c + 1], w16[4 * c + 2], w16[4 * c + 3]);
+  fence_proxy_async_smem();              // generic-proxy writes -> visible to the bulk copy
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(tm_g, buf, col, row0);
+    bulk_commit();
   }
 }
 
 template <bool kGrad>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 k_lmh_gemm(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
-           const LmhParams p) {
+           const __grid_constant__ CUtensorMap tm_g, const LmhParams p) {
   if (ld_status(p.status)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* aligned = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -274,11 +303,9 @@ k_lmh_gemm(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUt
       Acc a;
       acc_init(a);
       float4 cf = make_float4(0.f, 0.f, 0.f, 1.f);
-      __nv_bfloat16* grow = nullptr;
-      if constexpr (kGrad) {
-        cf = p.coef[lrow];
-        grow = p.grad + static_cast<size_t>(lrow) * p.ldg;
-      }
+      if constexpr (kGrad) cf = p.coef[lrow];
+      const int32_t brow0 = mb * kBM + q * 32;         // this warp's rows in the gradient
+      uint8_t* obuf = sm.out[warp - 2];
       for (int32_t nt = t0; nt < t1; ++nt, ++tc) {
         const uint32_t buf = tc & 1;
         if (!(ok = mbar_wait_warp(&sm.acc_full[buf], (tc >> 1) & 1, ab))) break;
@@ -288,18 +315,35 @@ k_lmh_gemm(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUt
         const int32_t nvalid = p.V - col0;             // columns < V from here
         uint32_t r0[32], r1[32];
         tmem_ld32x2(taddr, taddr + 32, r0, r1);
-        if constexpr (kGrad) grad64(r0, r1, cf, grow + col0, nvalid);
-        else fold64(a, r0, r1, nvalid);
+        if constexpr (kGrad) {
+          uint32_t o[32];
+          grad64(r0, r1, cf, o);
+          store_block(&tm_g, obuf, o, col0, brow0, p.V, lane, p.grad, p.ldg);
+          store_block(&tm_g, obuf, o + 16, col0 + 32, brow0, p.V, lane, p.grad, p.ldg);
+        } else {
+          fold64(a, r0, r1, nvalid);
+        }
         tmem_ld32x2(taddr + 64, taddr + 96, r0, r1);
         tc_fence_before();
         mbar_arrive(&sm.acc_empty[buf]); // the accumulator may be overwritten now
-        if constexpr (kGrad) grad64(r0, r1, cf, grow + col0 + 64, nvalid - 64);
-        else fold64(a, r0, r1, nvalid - 64);
+        if constexpr (kGrad) {
+          uint32_t o[32];
+          grad64(r0, r1, cf, o);
+          store_block(&tm_g, obuf, o, col0 + 64, brow0, p.V, lane, p.grad, p.ldg);
+          store_block(&tm_g, obuf, o + 16, col0 + 96, brow0, p.V, lane, p.grad, p.ldg);
+        } else {
+          fold64(a, r0, r1, nvalid - 64);
+        }
       }
       if (!ok) break;
       if constexpr (!kGrad)
         p.partial[static_cast<size_t>(chunk * 2 + half) * p.T_pad + lrow] =
             make_float4(a.m, a.s0 + a.s1, a.t0 + a.t1, a.mn);
+    }
+    if constexpr (kGrad) {
+      // the gradient stores must have landed before the CTA exits
+      if (lane == 0) bulk_wait_all();
+      __syncwarp();
     }
   }
   tc_fence_before();
@@ -503,7 +547,7 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_h, const CUtensorMap& tm_w, con
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < num_sms ? p.n_items : num_sms;
-  k_lmh_gemm<false><<<grid, kGemmThreads, smem, s>>>(tm_h, tm_w, p);
+  k_lmh_gemm<false><<<grid, kGemmThreads, smem, s>>>(tm_h, tm_w, tm_w, p);   // no gradient map
   k_lmh_combine<<<(T_pad + kCombineThreads - 1) / kCombineThreads, kCombineThreads, 0, s>>>(
       p.partial, 2 * p.n_chunks, T_pad, key_reach, lse, entropy, vmin, vmax, status);
   int launches = 2;
@@ -519,7 +563,8 @@ cudaError_t launch_lm_head(const CUtensorMap& tm_h, const CUtensorMap& tm_w, con
 }
 
 cudaError_t launch_lm_head_grad(const CUtensorMap& tm_h, const CUtensorMap& tm_w,
-                                const void* hidden, const void* weight, int32_t T_pad, int32_t H,
+                                const CUtensorMap& tm_g, const void* hidden, const void* weight,
+                                int32_t T_pad, int32_t H,
                                 int32_t V, int32_t row_lo, int32_t row_hi,
                                 const int32_t* token_ids, const int32_t* key_reach,
                                 const float* lse, const float* entropy, const float* g_lp,
@@ -549,7 +594,7 @@ cudaError_t launch_lm_head_grad(const CUtensorMap& tm_h, const CUtensorMap& tm_w
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   const int grid = p.n_items < num_sms ? p.n_items : num_sms;
-  k_lmh_gemm<true><<<grid, kGemmThreads, smem, s>>>(tm_h, tm_w, p);
+  k_lmh_gemm<true><<<grid, kGemmThreads, smem, s>>>(tm_h, tm_w, tm_g, p);
   int launches = 2;
   if (g_lp) {
     k_lmh_grad_labels<<<(rows + kLabelWarps - 1) / kLabelWarps, kLabelWarps * 32, 0, s>>>(

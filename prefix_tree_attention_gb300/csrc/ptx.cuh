@@ -136,6 +136,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
+// Store of a shared-memory box into global memory through a tensor map,
+// tracked by the issuing thread's bulk async-group (elements past the
+// tensor's extent are not written).  The box must keep its contents until
+// the group's reads are done (bulk_wait_read).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
 // Element-wise add of a shared-memory box into global memory through a
 // tensor map (fp32 add performed at L2), tracked by the issuing thread's bulk
 // async-group.  The smem box must keep its contents until the group's reads

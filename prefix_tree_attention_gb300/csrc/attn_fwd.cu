@@ -74,23 +74,45 @@ __device__ __forceinline__ float ex2(float x) {
 // Visibility bits of the 64 scores c2*64 .. c2*64+63 of a tile for query
 // row i, key j = j0 + column: bit e of vis[w] stands for column
 // c2*64 + 32*w + e and is set when j <= i <= reach[j].  The j <= i part is a
-// prefix of each 32-column group; the reach values are read four at a time
-// (every lane reads the same words, a broadcast).
+// prefix of each 32-column group.  For the reach part the warp lists the
+// group's distinct reach values, largest first, with the mask of the keys
+// that reach at least that far (one warp max and one ballot per value; the
+// keys of one node share one value, so a group rarely holds more than a
+// few); a row's mask is the one of the smallest listed value >= i.  A group
+// with more than kRuns values falls back to testing its keys one by one
+// (reach values read four at a time, a broadcast).  Warp-collective: every
+// lane holds a row of the same tile.
+constexpr int kRuns = 4;
+
 __device__ __forceinline__ void visible_bits(const int32_t* rch, int c2, int32_t j0, int32_t i,
                                              uint32_t (&vis)[2]) {
-  const int4* r4 = reinterpret_cast<const int4*>(rch) + c2 * 16;
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int w = 0; w < 2; ++w) {
-    const int32_t n = i - (j0 + c2 * 64 + w * 32) + 1;   // columns with j <= i
+    const int g = c2 * 2 + w;
+    const int32_t n = i - (j0 + g * 32) + 1;   // columns with j <= i
     const uint32_t pre = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : (1u << n) - 1u);
-    uint32_t rb = 0u;
+    const int32_t r = rch[g * 32 + lane];
+    uint32_t rb = 0u, left = 0xffffffffu;      // keys not yet listed (warp-uniform)
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int4 r = r4[w * 8 + q];
-      rb |= (i <= r.x ? 1u : 0u) << (4 * q);
-      rb |= (i <= r.y ? 1u : 0u) << (4 * q + 1);
-      rb |= (i <= r.z ? 1u : 0u) << (4 * q + 2);
-      rb |= (i <= r.w ? 1u : 0u) << (4 * q + 3);
+    for (int t = 0; t < kRuns; ++t) {
+      if (!left) break;
+      const int32_t v = __reduce_max_sync(0xffffffffu, ((left >> lane) & 1u) ? r : INT32_MIN);
+      const uint32_t m = __ballot_sync(0xffffffffu, r >= v);
+      if (i <= v) rb = m;
+      left = ~m;
+    }
+    if (left) {
+      rb = 0u;
+      const int4* r4 = reinterpret_cast<const int4*>(rch) + g * 8;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int4 x = r4[q];
+        rb |= (i <= x.x ? 1u : 0u) << (4 * q);
+        rb |= (i <= x.y ? 1u : 0u) << (4 * q + 1);
+        rb |= (i <= x.z ? 1u : 0u) << (4 * q + 2);
+        rb |= (i <= x.w ? 1u : 0u) << (4 * q + 3);
+      }
     }
     vis[w] = pre & rb;
   }

@@ -13,7 +13,7 @@
 
 namespace tree {
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const int32_t* key_reach, const void* blockmap, int32_t T_pad,
+                            const CUtensorMap& to, const int32_t* key_reach, const void* blockmap, int32_t T_pad,
                             int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o, float* lse,
                             int32_t* status, cudaStream_t s, int32_t row_lo, int32_t row_hi);
 size_t attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d);
@@ -85,13 +85,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Token-major [T, H, d] bf16 tensor viewed as a 3-D TMA map with a
-// 64-element (128-byte) x 1 head x 128-token box, 128-byte swizzle.
-bool encode_map(CUtensorMap* map, const void* base, int32_t T, int32_t H, int32_t d) {
+// 64-element (128-byte) x 1 head x box_rows-token box (128 for the operand
+// loads, 32 for the forward's per-warp O stores), 128-byte swizzle.
+bool encode_map(CUtensorMap* map, const void* base, int32_t T, int32_t H, int32_t d,
+                uint32_t box_rows = tree::kBlock) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(T)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(tree::kBlock)};
+  cuuint32_t box[3] = {64, 1, box_rows};
   cuuint32_t elem[3] = {1, 1, 1};
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
@@ -250,12 +252,12 @@ tree_status_t tree_attn_fwd(const void* q, const void* k, const void* v,
       !aligned16(key_reach) || !aligned16(blockmap))
     return TREE_ERR_ALIGNMENT;
   if (blockmap_bytes < tree_blockmap_bytes(T_pad)) return TREE_ERR_WORKSPACE;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
-      !encode_map(&tv, v, T_pad, Hkv, d))
+      !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&to, o, T_pad, Hq, d, 32))
     return TREE_ERR_CUDA;
-  return cuda_result(tree::launch_attn_fwd(tq, tk, tv, key_reach, blockmap, T_pad, Hq, Hkv, d,
-                                           scale, o, lse, dev_status, stream, 0, T_pad));
+  return cuda_result(tree::launch_attn_fwd(tq, tk, tv, to, key_reach, blockmap, T_pad, Hq, Hkv,
+                                           d, scale, o, lse, dev_status, stream, 0, T_pad));
 }
 
 size_t tree_attn_bwd_workspace_bytes(int32_t T_pad, int32_t Hq, int32_t d) {
@@ -390,10 +392,10 @@ tree_status_t tree_dta_attn(const void* q, const void* k, const void* v, const v
   const size_t bwd_bytes = tree::attn_bwd_workspace_bytes(T_pad, Hq, d);
   float* dk_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_bytes);
   float* dv_acc = dk_acc + static_cast<size_t>(T_pad) * Hkv * d;
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, to, tdo, tdq;
   if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
-      !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&tdo, d_o, T_pad, Hq, d) ||
-      !encode_map_acc(&tdq, workspace, T_pad, Hq, d))
+      !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&to, o, T_pad, Hq, d, 32) ||
+      !encode_map(&tdo, d_o, T_pad, Hq, d) || !encode_map_acc(&tdq, workspace, T_pad, Hq, d))
     return TREE_ERR_CUDA;
   const int sms = num_sms_current();
   cudaError_t e = tree::launch_dta_init(o, dq, lse, workspace,
@@ -402,8 +404,8 @@ tree_status_t tree_dta_attn(const void* q, const void* k, const void* v, const v
   for (int64_t i = 0; e == cudaSuccess && i < n_ops; ++i) {
     const int32_t kind = ops[3 * i], t0 = ops[3 * i + 1], t1 = ops[3 * i + 2];
     if (kind != TREE_DTA_BWD_POP)     // forward of the rows against their visible keys
-      e = tree::launch_attn_fwd(tq, tk, tv, key_reach, blockmap, T_pad, Hq, Hkv, d, scale, o,
-                                lse, dev_status, stream, t0, t1);
+      e = tree::launch_attn_fwd(tq, tk, tv, to, key_reach, blockmap, T_pad, Hq, Hkv, d, scale,
+                                o, lse, dev_status, stream, t0, t1);
     if (e == cudaSuccess && kind != TREE_DTA_FWD_PUSH) {   // backward of the rows
       e = tree::launch_attn_bwd_prepare(o, d_o, lse, T_pad, Hq, d, workspace, dev_status,
                                         stream, sms, t0, t1);

@@ -289,7 +289,8 @@ template <int D>
 __global__ void __launch_bounds__(kFwdThreads, 1)
 tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   if (ld_status(p.status)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* aligned = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -474,7 +475,47 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
       // inside the window store)
       const bool in_window = i >= p.row_lo && i < p.row_hi;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(i) * p.Hq + h) * D;
-      if (ok && ntiles > 0 && mbar_wait_warp(&sm.o_full[t], (ntiles - 1) & 1, ab)) {
+      const bool have_o = ok && ntiles > 0 && mbar_wait_warp(&sm.o_full[t], (ntiles - 1) & 1, ab);
+      if (have_o && !p.windowed) {
+        // O through shared memory: this slot's Q tile, which its last QK has
+        // finished reading, takes the normalised rows in the Q tile's own
+        // 128-byte-swizzled layout; one lane then writes the warp's 32 rows
+        // with a bulk tensor store per 64-column half (a thread's direct
+        // stores would touch 32 rows of O per instruction).
+        tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        uint8_t* stage = reinterpret_cast<uint8_t*>(sm.q[t]);
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t reg[32];
+          tmem_ld32(o_addr + c4 * 32, reg);
+          uint8_t* row = stage + (c4 >> 1) * (kBlock * 128) + r * 128;
+#pragma unroll
+          for (int e8 = 0; e8 < 4; ++e8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 0]) * inv_l, __uint_as_float(reg[e8 * 8 + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 2]) * inv_l, __uint_as_float(reg[e8 * 8 + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 4]) * inv_l, __uint_as_float(reg[e8 * 8 + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(reg[e8 * 8 + 6]) * inv_l, __uint_as_float(reg[e8 * 8 + 7]) * inv_l);
+            const int chunk = (c4 & 1) * 4 + e8;
+            *reinterpret_cast<uint4*>(row + ((chunk ^ (r & 7)) << 4)) = w;
+          }
+        }
+        fence_proxy_async_smem();        // generic-proxy writes -> visible to the bulk copy
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int hf = 0; hf < kHalves; ++hf)
+            tma_store_3d(&tm_o, stage + hf * (kBlock * 128) + quarter * 32 * 128, hf * 64, h,
+                         qa * kBlock + quarter * 32);
+          bulk_commit();
+          bulk_wait_read();              // the tile must outlive the copy's reads
+        }
+        __syncwarp();
+        p.lse[static_cast<size_t>(h) * p.T_pad + i] =
+            l > 0.f ? m * 0.69314718055994531f + logf(l) : -INFINITY;
+      } else if (have_o) {
+        // a window may start or end inside the warp's rows: direct stores
         tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
@@ -513,13 +554,13 @@ tree_attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 
 template <int D>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdParams& p, int grid, cudaStream_t s) {
+                         const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t s) {
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
   cudaError_t e = cudaFuncSetAttribute(tree_attn_fwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  tree_attn_fwd_kernel<D><<<grid, kFwdThreads, smem, s>>>(tq, tk, tv, p);
+  tree_attn_fwd_kernel<D><<<grid, kFwdThreads, smem, s>>>(tq, tk, tv, to, p);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -527,7 +568,7 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const int32_t* key_reach, const void* blockmap, int32_t T_pad,
+                            const CUtensorMap& to, const int32_t* key_reach, const void* blockmap, int32_t T_pad,
                             int32_t Hq, int32_t Hkv, int32_t d, float scale, void* o, float* lse,
                             int32_t* status, cudaStream_t s, int32_t row_lo, int32_t row_hi) {
   const int g = Hq / Hkv;
@@ -551,8 +592,8 @@ cudaError_t launch_attn_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const 
   p.n_qa = row_hi > row_lo ? (row_hi - 1) / kBlock - p.qa_lo + 1 : 0;
   if (p.n_qa == 0) return cudaSuccess;
   const int grid = p.n_qa * p.n_hgroups;
-  return d == 64 ? launch_fwd_d<64>(tq, tk, tv, p, grid, s)
-                 : launch_fwd_d<128>(tq, tk, tv, p, grid, s);
+  return d == 64 ? launch_fwd_d<64>(tq, tk, tv, to, p, grid, s)
+                 : launch_fwd_d<128>(tq, tk, tv, to, p, grid, s);
 }
 
 }  // namespace tree

@@ -23,7 +23,8 @@ cudaError_t launch_attn_bwd_prepare(const void* o, const void* d_o, const float*
                                     int32_t row_hi);
 cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo,
-                                 const CUtensorMap& tdq, const int32_t* key_reach,
+                                 const CUtensorMap& tdq, const CUtensorMap& tdk,
+                                 const CUtensorMap& tdv, const int32_t* key_reach,
                                  const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
                                  int32_t d, float scale, void* dk, void* dv, void* workspace,
                                  int32_t* status, cudaStream_t s, int num_sms, int32_t row_lo,
@@ -300,15 +301,16 @@ tree_status_t tree_attn_bwd_main(const void* q, const void* k, const void* v, co
     if (!aligned16(p)) return TREE_ERR_ALIGNMENT;
   if (workspace_bytes < tree::attn_bwd_workspace_bytes(T_pad, Hq, d)) return TREE_ERR_WORKSPACE;
   if (blockmap_bytes < tree_blockmap_bytes(T_pad)) return TREE_ERR_WORKSPACE;
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
       !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&tdo, d_o, T_pad, Hq, d) ||
-      !encode_map_acc(&tdq, workspace, T_pad, Hq, d))   // the accumulator leads the workspace
+      !encode_map_acc(&tdq, workspace, T_pad, Hq, d) ||   // the accumulator leads the workspace
+      !encode_map(&tdk, dk, T_pad, Hkv, d, 32) || !encode_map(&tdv, dv, T_pad, Hkv, d, 32))
     return TREE_ERR_CUDA;
-  return cuda_result(tree::launch_attn_bwd_main(tq, tk, tv, tdo, tdq, key_reach, blockmap, T_pad,
-                                                Hq, Hkv, d, scale, dk, dv, workspace, dev_status,
-                                                stream, num_sms_current(), 0, T_pad, nullptr,
-                                                nullptr));
+  return cuda_result(tree::launch_attn_bwd_main(tq, tk, tv, tdo, tdq, tdk, tdv, key_reach,
+                                                blockmap, T_pad, Hq, Hkv, d, scale, dk, dv,
+                                                workspace, dev_status, stream, num_sms_current(),
+                                                0, T_pad, nullptr, nullptr));
 }
 
 tree_status_t tree_attn_bwd_finish(int32_t T_pad, int32_t Hq, int32_t d, float scale,
@@ -392,10 +394,11 @@ tree_status_t tree_dta_attn(const void* q, const void* k, const void* v, const v
   const size_t bwd_bytes = tree::attn_bwd_workspace_bytes(T_pad, Hq, d);
   float* dk_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + bwd_bytes);
   float* dv_acc = dk_acc + static_cast<size_t>(T_pad) * Hkv * d;
-  CUtensorMap tq, tk, tv, to, tdo, tdq;
+  CUtensorMap tq, tk, tv, to, tdo, tdq, tdk, tdv;
   if (!encode_map(&tq, q, T_pad, Hq, d) || !encode_map(&tk, k, T_pad, Hkv, d) ||
       !encode_map(&tv, v, T_pad, Hkv, d) || !encode_map(&to, o, T_pad, Hq, d, 32) ||
-      !encode_map(&tdo, d_o, T_pad, Hq, d) || !encode_map_acc(&tdq, workspace, T_pad, Hq, d))
+      !encode_map(&tdo, d_o, T_pad, Hq, d) || !encode_map_acc(&tdq, workspace, T_pad, Hq, d) ||
+      !encode_map(&tdk, dk, T_pad, Hkv, d, 32) || !encode_map(&tdv, dv, T_pad, Hkv, d, 32))
     return TREE_ERR_CUDA;
   const int sms = num_sms_current();
   cudaError_t e = tree::launch_dta_init(o, dq, lse, workspace,
@@ -410,9 +413,9 @@ tree_status_t tree_dta_attn(const void* q, const void* k, const void* v, const v
       e = tree::launch_attn_bwd_prepare(o, d_o, lse, T_pad, Hq, d, workspace, dev_status,
                                         stream, sms, t0, t1);
       if (e == cudaSuccess)
-        e = tree::launch_attn_bwd_main(tq, tk, tv, tdo, tdq, key_reach, blockmap, T_pad, Hq,
-                                       Hkv, d, scale, dk, dv, workspace, dev_status, stream,
-                                       sms, t0, t1, dk_acc, dv_acc);
+        e = tree::launch_attn_bwd_main(tq, tk, tv, tdo, tdq, tdk, tdv, key_reach, blockmap,
+                                       T_pad, Hq, Hkv, d, scale, dk, dv, workspace, dev_status,
+                                       stream, sms, t0, t1, dk_acc, dv_acc);
       if (e == cudaSuccess)
         e = tree::launch_attn_bwd_finish(T_pad, Hq, d, scale, workspace, dq, dev_status, stream,
                                          sms, t0, t1);

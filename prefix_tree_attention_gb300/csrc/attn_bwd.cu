@@ -117,7 +117,9 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_do,
-                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                     const __grid_constant__ CUtensorMap tm_dq,
+                     const __grid_constant__ CUtensorMap tm_dk,
+                     const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   if (ld_status(p.status)) return;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {          // the layout needs 1024-byte alignment
@@ -477,6 +479,44 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
           }
         }
       }
+    } else if (D == 128 && ok && nsteps > 0 &&
+               mbar_wait_warp(&sm.dvdk_done, (nsteps - 1) & 1, ab)) {
+      // dV and dK through shared memory: the resident V and K tiles, whose
+      // last readers (MMAs) have completed, take this warp's 32 rows of its
+      // 64-column half in their own 128-byte-swizzled layout; one lane then
+      // writes each with a bulk tensor store.
+      tc_fence_after();
+      uint8_t* sv = reinterpret_cast<uint8_t*>(sm.v) + w * (kBlock * 128);
+      uint8_t* sk = reinterpret_cast<uint8_t*>(sm.k) + w * (kBlock * 128);
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t rv[32], rk[32];
+        tmem_ld32x2(tbase + lane_off + kDV + w * 64 + c2 * 32,
+                    tbase + lane_off + kDK + w * 64 + c2 * 32, rv, rk);
+#pragma unroll
+        for (int e8 = 0; e8 < 4; ++e8) {
+          const float* fv = reinterpret_cast<const float*>(rv + e8 * 8);
+          const float* fk = reinterpret_cast<const float*>(rk + e8 * 8);
+          const uint32_t off = r * 128 + (((c2 * 4 + e8) ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(sv + off) =
+              make_uint4(pack_bf16x2(fv[0], fv[1]), pack_bf16x2(fv[2], fv[3]),
+                         pack_bf16x2(fv[4], fv[5]), pack_bf16x2(fv[6], fv[7]));
+          *reinterpret_cast<uint4*>(sk + off) =
+              make_uint4(pack_bf16x2(fk[0] * p.scale, fk[1] * p.scale),
+                         pack_bf16x2(fk[2] * p.scale, fk[3] * p.scale),
+                         pack_bf16x2(fk[4] * p.scale, fk[5] * p.scale),
+                         pack_bf16x2(fk[6] * p.scale, fk[7] * p.scale));
+        }
+      }
+      fence_proxy_async_smem();          // generic-proxy writes -> visible to the bulk copy
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&tm_dv, sv + quarter * 32 * 128, w * 64, kvh, kb * kBlock + quarter * 32);
+        tma_store_3d(&tm_dk, sk + quarter * 32 * 128, w * 64, kvh, kb * kBlock + quarter * 32);
+        bulk_commit();
+        bulk_wait_read();                // the tiles must outlive the copies' reads
+      }
+      __syncwarp();
     } else if (ok && nsteps > 0 && mbar_wait_warp(&sm.dvdk_done, (nsteps - 1) & 1, ab)) {
       tc_fence_after();
 #pragma unroll
@@ -616,7 +656,8 @@ cudaError_t launch_attn_bwd_prepare(const void* o, const void* d_o, const float*
 
 cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                                  const CUtensorMap& tv, const CUtensorMap& tdo,
-                                 const CUtensorMap& tdq, const int32_t* key_reach,
+                                 const CUtensorMap& tdq, const CUtensorMap& tdk,
+                                 const CUtensorMap& tdv, const int32_t* key_reach,
                                  const void* blockmap, int32_t T_pad, int32_t Hq, int32_t Hkv,
                                  int32_t d, float scale, void* dk, void* dv, void* workspace,
                                  int32_t* status, cudaStream_t s, int num_sms, int32_t row_lo,
@@ -652,14 +693,14 @@ cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
                              static_cast<int>(sizeof(BwdSmem<64>)));
     if (e != cudaSuccess) return e;
     tree_attn_bwd_kernel<64><<<grid, kBwdThreads, sizeof(BwdSmem<64>), s>>>(tq, tk, tv, tdo, tdq,
-                                                                          p);
+                                                                          tdk, tdv, p);
   } else {
     e = cudaFuncSetAttribute(tree_attn_bwd_kernel<128>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(BwdSmem<128>)));
     if (e != cudaSuccess) return e;
     tree_attn_bwd_kernel<128><<<grid, kBwdThreads, sizeof(BwdSmem<128>), s>>>(tq, tk, tv, tdo,
-                                                                            tdq, p);
+                                                                            tdq, tdk, tdv, p);
   }
   count_launches(1);
   return cudaGetLastError();

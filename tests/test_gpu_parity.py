@@ -260,6 +260,21 @@ def test_random_tries_dense(Hq, Hkv, d, seed):
         check_integer_outputs(p, bufs)
 
 
+@pytest.mark.parametrize("Hq,Hkv,d", [(4, 2, 128), (2, 2, 64)])
+def test_key_block_with_many_reach_values(Hq, Hkv, d):
+    # A chain of twenty 5-token nodes, each also the parent of a 200-token
+    # leaf: the first key block holds twenty distinct reach values, more
+    # than 4 in every 32-key group, so the forward's visibility bits of its
+    # PARTIAL tiles take the key-by-key fallback instead of the run list.
+    seqs = [list(range(1, 5 * k + 1)) + [1000 * k + t for t in range(200)] for k in range(1, 21)]
+    _, (p,) = pack_both(seqs, 8192)
+    reach = expected_reach(p)
+    groups = [len(set(reach[g * 32:g * 32 + 32].tolist())) for g in range(3)]
+    assert min(groups) > 4
+    bufs = check_attention_dense(p, Hq, Hkv, d, seed=6)
+    check_integer_outputs(p, bufs)
+
+
 @pytest.mark.parametrize("Hq,Hkv,d", [(4, 1, 128), (2, 2, 64)])
 def test_top_level_boundaries_inside_blocks(Hq, Hkv, d):
     # Several top-level subtrees whose boundaries fall inside 128-token

@@ -54,6 +54,9 @@ constexpr uint32_t kRegsDq = 96, kRegsEw = 168, kRegsCtl = 72;
 static_assert(128 * kRegsDq + 256 * kRegsEw + 128 * kRegsCtl <= kBwdThreads * 128,
               "register split exceeds the launch allocation");
 constexpr int kWarpProducer = 12, kWarpMma = 13, kWarpEw0 = 4;
+// Query blocks of a key block's column one CTA walks in the fp32-accumulate
+// (windowed stack-gradient) mode.
+constexpr int kSplitQ = 4;
 
 template <int D>
 struct __align__(1024) BwdSmem {
@@ -141,10 +144,12 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   // CTAs take the kv heads in reverse, starting with the one whose heavy
   // columns ran last.  Each thread tests one or more columns; the counts
   // are summed by the prologue barrier(s) below.
+  const bool accumulate = p.dk_acc != nullptr;
   const int32_t heavy_len = bm.base[1] / (p.num_sms > 0 ? p.num_sms : 1);
   int heavy_local = 0;
-  for (int32_t k = threadIdx.x; k < p.nb; k += kBwdThreads)
-    heavy_local += (bm.col_hi()[k] - k + 1) > heavy_len;
+  if (!accumulate)
+    for (int32_t k = threadIdx.x; k < p.nb; k += kBwdThreads)
+      heavy_local += (bm.col_hi()[k] - k + 1) > heavy_len;
   AbortState ab{&sm.abort_flag, p.status};
 
   if (threadIdx.x == 0) {
@@ -164,26 +169,39 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     mbar_init(&sm.drain, 1);
     fence_mbar_init();
   }
-  int32_t heavy_n = __syncthreads_count(heavy_local > 0);
-  for (int i = 1; i * kBwdThreads < p.nb; ++i) heavy_n += __syncthreads_count(heavy_local > i);
-  int32_t kvh, rank;
-  if (static_cast<int32_t>(blockIdx.x) < heavy_n * p.Hkv) {
-    kvh = blockIdx.x / heavy_n;
-    rank = blockIdx.x % heavy_n;
+  int32_t kvh, kb, qlo_c, qhi_c;         // the query blocks this CTA may walk
+  if (accumulate) {
+    const int32_t qlo = p.row_lo / kBlock, qhi = (p.row_hi - 1) / kBlock;
+    const int32_t nsplit = (qhi - qlo + kSplitQ) / kSplitQ;
+    const int32_t per_kv = (qhi + 1) * nsplit;
+    kvh = blockIdx.x / per_kv;
+    const int32_t rem = blockIdx.x % per_kv, c = rem % nsplit;
+    kb = rem / nsplit;
+    qlo_c = qlo + c * kSplitQ;
+    qhi_c = min(qhi, qlo_c + kSplitQ - 1);
   } else {
-    const int32_t j = blockIdx.x - heavy_n * p.Hkv, nl = p.nb - heavy_n;
-    kvh = p.Hkv - 1 - j / nl;
-    rank = heavy_n + j % nl;
+    int32_t heavy_n = __syncthreads_count(heavy_local > 0);
+    for (int i = 1; i * kBwdThreads < p.nb; ++i) heavy_n += __syncthreads_count(heavy_local > i);
+    int32_t rank;
+    if (static_cast<int32_t>(blockIdx.x) < heavy_n * p.Hkv) {
+      kvh = blockIdx.x / heavy_n;
+      rank = blockIdx.x % heavy_n;
+    } else {
+      const int32_t j = blockIdx.x - heavy_n * p.Hkv, nl = p.nb - heavy_n;
+      kvh = p.Hkv - 1 - j / nl;
+      rank = heavy_n + j % nl;
+    }
+    kb = bm.col_order()[rank];
+    if (!dcheck(kb >= 0 && kb < p.nb, p.status)) return;    // CTA-uniform, before TMEM
+    qlo_c = p.row_lo / kBlock;
+    qhi_c = (p.row_hi - 1) / kBlock;
   }
-  const int32_t kb = bm.col_order()[rank];
-  if (!dcheck(kb >= 0 && kb < p.nb, p.status)) return;    // CTA-uniform, before TMEM
+  // the key block's column run kb..col_hi, clipped to those query blocks
+  const int32_t qa_first = max(kb, qlo_c);
+  const int32_t qa_last = min(bm.col_hi()[kb], qhi_c);
   const int32_t col_full_hi = bm.col_full_hi()[kb];
-  // the key block's column run kb..col_hi, clipped to the window's blocks
-  const int32_t qa_first = max(kb, p.row_lo / kBlock);
-  const int32_t qa_last = min(bm.col_hi()[kb], (p.row_hi - 1) / kBlock);
   const int32_t col_len = qa_last >= qa_first ? qa_last - qa_first + 1 : 0;
   const int32_t nsteps = col_len * g;
-  const bool accumulate = p.dk_acc != nullptr;
   if (accumulate && nsteps == 0) return;     // CTA-uniform: nothing to add
   if (warp == kWarpMma) {
     tmem_alloc(&sm.tmem_slot, 512);
@@ -450,8 +468,8 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     __nv_bfloat16* dvrow = p.dv + row_off;
     __nv_bfloat16* dkrow = p.dk + row_off;
     if (accumulate) {
-      // fp32 read-add-write of this key row's half: within one launch each
-      // (key, kv head) row belongs to exactly one CTA, so no atomics
+      // fp32 vector atomic adds of this key row's half: the CTAs of one key
+      // block's column chunks add into the same rows
       if (ok && mbar_wait_warp(&sm.dvdk_done, (nsteps - 1) & 1, ab)) {
         tc_fence_after();
         float* av = p.dv_acc + row_off;
@@ -463,19 +481,13 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       tbase + lane_off + kDK + w * (D / 2) + c2 * 32, rv, rk);
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
-            float4* pv4 = reinterpret_cast<float4*>(av + c2 * 32 + e4 * 4);
-            float4* pk4 = reinterpret_cast<float4*>(ak + c2 * 32 + e4 * 4);
-            float4 a = *pv4, b = *pk4;
-            a.x += __uint_as_float(rv[4 * e4]);
-            a.y += __uint_as_float(rv[4 * e4 + 1]);
-            a.z += __uint_as_float(rv[4 * e4 + 2]);
-            a.w += __uint_as_float(rv[4 * e4 + 3]);
-            b.x += __uint_as_float(rk[4 * e4]) * p.scale;
-            b.y += __uint_as_float(rk[4 * e4 + 1]) * p.scale;
-            b.z += __uint_as_float(rk[4 * e4 + 2]) * p.scale;
-            b.w += __uint_as_float(rk[4 * e4 + 3]) * p.scale;
-            *pv4 = a;
-            *pk4 = b;
+            red_add_v4(av + c2 * 32 + e4 * 4, __uint_as_float(rv[4 * e4]),
+                       __uint_as_float(rv[4 * e4 + 1]), __uint_as_float(rv[4 * e4 + 2]),
+                       __uint_as_float(rv[4 * e4 + 3]));
+            red_add_v4(ak + c2 * 32 + e4 * 4, __uint_as_float(rk[4 * e4]) * p.scale,
+                       __uint_as_float(rk[4 * e4 + 1]) * p.scale,
+                       __uint_as_float(rk[4 * e4 + 2]) * p.scale,
+                       __uint_as_float(rk[4 * e4 + 3]) * p.scale);
           }
         }
       }
@@ -685,7 +697,10 @@ cudaError_t launch_attn_bwd_main(const CUtensorMap& tq, const CUtensorMap& tk,
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = status;
-  const int grid = p.nb * Hkv;
+  // accumulate mode: (kv head, key block up to the window's last query
+  // block, chunk of kSplitQ window query blocks); else (kv head, key block)
+  const int32_t qlo = row_lo / kBlock, qhi = (row_hi - 1) / kBlock;
+  const int grid = dk_acc ? Hkv * (qhi + 1) * ((qhi - qlo + kSplitQ) / kSplitQ) : p.nb * Hkv;
   cudaError_t e;
   if (d == 64) {
     e = cudaFuncSetAttribute(tree_attn_bwd_kernel<64>,

@@ -97,6 +97,14 @@ struct BwdParams {
   int32_t* status;
 };
 
+// Fire-and-forget fp32 vector atomic add of four consecutive floats
+// (16-byte aligned): the accumulate-mode dK/dV epilogue.
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

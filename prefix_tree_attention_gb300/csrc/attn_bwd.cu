@@ -576,38 +576,57 @@ tree_attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
 }
 
-// a4: D rows, lse2 rows, zeroed dQ accumulator.  One warp per (token, head).
+// a4: D rows, lse2 rows, zeroed dQ accumulator.
 template <int D>
 __global__ void __launch_bounds__(256)
 tree_attn_bwd_prep_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse,
                           float* dd, float* lse2, float* dq_acc, int32_t T_pad, int32_t Hq,
                           int32_t row_lo, int32_t row_hi, const int32_t* status) {
   if (ld_status(status)) return;
-  // (token, head) rows of the token window [row_lo, row_hi)
-  const int64_t rows = static_cast<int64_t>(row_hi) * Hq;
+  // One warp per (group of 8 consecutive tokens, head), heads inner: the
+  // warps of a token group read consecutive 256-byte rows of O and dO, and
+  // each warp reads and writes its head's 8 LSE / D entries as one 32-byte
+  // sector (the per-head arrays are [Hq, T_pad]).
   const int lane = threadIdx.x & 31;
-  for (int64_t row = static_cast<int64_t>(row_lo) * Hq +
-                     ((blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5);
-       row < rows; row += (int64_t(gridDim.x) * blockDim.x) >> 5) {
-    const int64_t i = row / Hq, h = row % Hq;
-    constexpr int kPer = D / 32;     // elements per lane (2 or 4)
-    float acc = 0.f;
-    const __nv_bfloat16* po = o + row * D + lane * kPer;
-    const __nv_bfloat16* pd = dout + row * D + lane * kPer;
+  const int32_t g_lo = row_lo >> 3, g_hi = (row_hi + 7) >> 3;
+  const int64_t items = static_cast<int64_t>(g_hi - g_lo) * Hq;
+  constexpr int kPer = D / 32;     // elements per lane (2 or 4)
+  for (int64_t it = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; it < items;
+       it += (int64_t(gridDim.x) * blockDim.x) >> 5) {
+    const int32_t grp = g_lo + static_cast<int32_t>(it / Hq), h = static_cast<int32_t>(it % Hq);
+    float acc[8];
 #pragma unroll
-    for (int e = 0; e < kPer; e += 2) {
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(po + e));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(pd + e));
-      acc += a.x * b.x + a.y * b.y;
+    for (int r = 0; r < 8; ++r) {
+      const int32_t i = grp * 8 + r;
+      acc[r] = 0.f;
+      if (i < row_lo || i >= row_hi) continue;           // warp-uniform
+      const int64_t row = static_cast<int64_t>(i) * Hq + h;
+      const __nv_bfloat16* po = o + row * D + lane * kPer;
+      const __nv_bfloat16* pd = dout + row * D + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; e += 2) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(po + e));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(pd + e));
+        acc[r] += a.x * b.x + a.y * b.y;
+      }
+      float4* z = reinterpret_cast<float4*>(dq_acc + row * D);
+      for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    float4* z = reinterpret_cast<float4*>(dq_acc + row * D);
-    for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane == 0) {
-      // stored negated so the main kernel's paired FMA/add consume them directly
-      dd[h * T_pad + i] = -acc;
-      lse2[h * T_pad + i] = -lse[h * T_pad + i] * 1.4426950408889634f;
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+    if (lane < 8) {
+      const int32_t i = grp * 8 + lane;
+      float mine = acc[0];
+#pragma unroll
+      for (int r = 1; r < 8; ++r) mine = lane == r ? acc[r] : mine;
+      if (i >= row_lo && i < row_hi) {
+        // stored negated so the main kernel's paired FMA/add consume them directly
+        const int64_t hi = static_cast<int64_t>(h) * T_pad + i;
+        dd[hi] = -mine;
+        lse2[hi] = -lse[hi] * 1.4426950408889634f;
+      }
     }
   }
 }
@@ -660,8 +679,8 @@ cudaError_t launch_attn_bwd_prepare(const void* o, const void* d_o, const float*
                                     int32_t row_lo, int32_t row_hi) {
   BwdWorkspace w = carve(workspace, T_pad, Hq, d);
   if (row_hi <= row_lo) return cudaSuccess;
-  const int64_t rows = static_cast<int64_t>(row_hi - row_lo) * Hq;
-  const int blocks = grid_cap((rows * 32 + 255) / 256, num_sms);
+  const int64_t items = static_cast<int64_t>(((row_hi + 7) >> 3) - (row_lo >> 3)) * Hq;
+  const int blocks = grid_cap((items * 32 + 255) / 256, num_sms);
   const auto* po = static_cast<const __nv_bfloat16*>(o);
   const auto* pd = static_cast<const __nv_bfloat16*>(d_o);
   if (d == 64)

@@ -12,7 +12,11 @@
 // Along any root path the set of sequences passing a child is a subset of
 // the set passing its parent, so "identical sets" is tested as "equal
 // counts".  Children keep first-insertion order (a linked list appended at
-// the tail); FFD ties keep input order.
+// the tail); FFD ties keep input order.  A child is found by walking its
+// parent's list while the parent has few children (most nodes of a trie of
+// token sequences have one) and through a hash map once it has many; each
+// sequence's node path is recorded as it is inserted, so its packed indices
+// need no second walk.
 #include <algorithm>
 #include <cstdint>
 #include <memory>
@@ -31,13 +35,19 @@ struct UNode {            // uncompressed node: one token
   int32_t last_child = -1;
   int32_t next_sibling = -1;
   int32_t pass = 0;       // sequences passing this node
+  int32_t nkids = 0;
 };
+
+// Children of a node with at least this many are also kept in the hash map.
+constexpr int32_t kHashKids = 8;
 
 struct UTrie {
   std::vector<UNode> nodes;                    // nodes[0] is the virtual root
-  std::unordered_map<uint64_t, int32_t> child; // (parent, tok) -> node
+  std::unordered_map<uint64_t, int32_t> child; // (parent, tok) -> node, wide nodes only
   int64_t occupied = 0;
   std::vector<int32_t> seqs;                   // input indices, insertion order
+  std::vector<int32_t> path;                   // every sequence's nodes, in order
+  std::vector<int64_t> path_off{0};            // sequence k: path[path_off[k], path_off[k+1])
 
   UTrie() { nodes.push_back(UNode{-1, -1}); }
 
@@ -46,8 +56,13 @@ struct UTrie {
            static_cast<uint32_t>(tok);
   }
   int32_t find(int32_t parent, int32_t tok) const {
-    auto it = child.find(key(parent, tok));
-    return it == child.end() ? -1 : it->second;
+    if (nodes[parent].nkids >= kHashKids) {
+      auto it = child.find(key(parent, tok));
+      return it == child.end() ? -1 : it->second;
+    }
+    for (int32_t c = nodes[parent].first_child; c >= 0; c = nodes[c].next_sibling)
+      if (nodes[c].tok == tok) return c;
+    return -1;
   }
   int64_t additional(const int32_t* s, int64_t len) const {
     int32_t u = 0;
@@ -67,16 +82,24 @@ struct UTrie {
       if (c < 0) {
         c = static_cast<int32_t>(nodes.size());
         nodes.push_back(UNode{s[i], u});
-        child.emplace(key(u, s[i]), c);
-        if (nodes[u].last_child < 0) nodes[u].first_child = c;
-        else nodes[nodes[u].last_child].next_sibling = c;
-        nodes[u].last_child = c;
+        UNode& p = nodes[u];
+        if (p.last_child < 0) p.first_child = c;
+        else nodes[p.last_child].next_sibling = c;
+        p.last_child = c;
+        if (++p.nkids == kHashKids) {       // the node turns wide: index all its children
+          for (int32_t k = p.first_child; k >= 0; k = nodes[k].next_sibling)
+            child.emplace(key(u, nodes[k].tok), k);
+        } else if (p.nkids > kHashKids) {
+          child.emplace(key(u, s[i]), c);
+        }
         ++occupied;
       }
       nodes[c].pass += 1;
+      path.push_back(c);
       u = c;
     }
     seqs.push_back(sid);
+    path_off.push_back(static_cast<int64_t>(path.size()));
   }
 };
 
@@ -94,8 +117,7 @@ struct tree_packing {
 
 namespace {
 
-void lay_out(const UTrie& u, const int32_t* tokens, const int64_t* offs, int32_t block,
-             int32_t pad_to, tree_packing::Trie& out) {
+void lay_out(const UTrie& u, int32_t block, int32_t pad_to, tree_packing::Trie& out) {
   // Compressed nodes: chains of uncompressed nodes.
   struct CNode {
     std::vector<int32_t> chain;
@@ -186,16 +208,10 @@ void lay_out(const UTrie& u, const int32_t* tokens, const int64_t* offs, int32_t
   out.seq_ids = u.seqs;
   out.seq_idx.resize(u.seqs.size());
   for (size_t k = 0; k < u.seqs.size(); ++k) {
-    int32_t sid = u.seqs[k];
-    const int32_t* s = tokens + offs[sid];
-    int64_t len = offs[sid + 1] - offs[sid];
+    const int64_t a = u.path_off[k], len = u.path_off[k + 1] - a;
     auto& idx = out.seq_idx[k];
     idx.resize(len);
-    int32_t x = 0;
-    for (int64_t i = 0; i < len; ++i) {
-      x = u.find(x, s[i]);
-      idx[i] = upos[x];
-    }
+    for (int64_t i = 0; i < len; ++i) idx[i] = upos[u.path[a + i]];
   }
 }
 
@@ -242,8 +258,7 @@ tree_status_t tree_packing_build(const int32_t* tokens, const int64_t* seq_offse
   if (!pk) return TREE_ERR_INVALID_ARG;
   pk->tries.resize(tries.size());
   for (size_t t = 0; t < tries.size(); ++t)
-    lay_out(*tries[t], tokens, seq_offsets, block, pad_to_max ? max_tokens_per_mb : 0,
-            pk->tries[t]);
+    lay_out(*tries[t], block, pad_to_max ? max_tokens_per_mb : 0, pk->tries[t]);
   *out = pk;
   return TREE_OK;
 }

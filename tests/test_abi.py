@@ -255,6 +255,24 @@ def test_packer_random_small_sets():
             assert a.visible_pairs == OM.visible_pairs(b)
 
 
+def test_packer_wide_nodes():
+    # A root and a shared prefix with 20 distinct continuations each, with
+    # repeats, so that children are looked up before and after a node gets
+    # more than a handful of them (the packer then also indexes them by hash).
+    rng = W.SplitMix64(99)
+    seqs = []
+    for rep in range(3):
+        for c in range(20):
+            seqs.append([7, 7, 7, 100 + c] + [rng.randint(1, 3) for _ in range(rng.randint(1, 6))])
+            seqs.append([500 + c] + [rng.randint(1, 3) for _ in range(rng.randint(1, 6))])
+    for cap in (128, 1024):
+        mine = ptg.pack_sequences(seqs, cap)
+        ref = OT.pack_sequences(seqs, cap)
+        _same_packing(mine, ref)
+        for a, b in zip(mine, ref):
+            assert a.visible_pairs == OM.visible_pairs(b)
+
+
 def test_packer_pad_to_max():
     seqs = W.sequences("tiny")
     mine = ptg.pack_sequences(seqs, 2048, pad_to_max=True)
